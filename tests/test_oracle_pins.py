@@ -1,0 +1,301 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+- brute force in torch fp64 (dense mask, softmax, autograd) on tiny inputs;
+- central finite differences of the oracle's own forward for the gradients;
+- invariants the method's definition fixes (constant V, a single attended key,
+  fully masked rows, D = dO.O, invariance of O and dQ under a shift of every key);
+- closed forms: attended-pair counts and the tile counts of causal masks
+  ("about half of the GEMMs skipped", blog "FlashMask技术" §1 item 2 and §2.2);
+- the pages' worked examples (blog §2.1 causal row form, §3.3 document packing)
+  stored under tests/golden/.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_fm_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _mask_np(wl, seed=0):
+    return W.make_mask(wl, seed)
+
+
+def _bounds(m, b=0, hm=0):
+    return [m[k][b, hm] for k in ("lts", "lte", "uts", "ute")]
+
+
+def _rand_mask(N, rng, Hm=1, B=1):
+    """Arbitrary column bounds: empty, reversed, overlapping and whole-column ranges."""
+    a = rng.integers(0, N + 1, size=(4, B, Hm, N)).astype(np.int32)
+    return dict(lts=a[0], lte=a[1], uts=a[2], ute=a[3])
+
+
+def _torch_reference(q, k, v, dO, M, scale):
+    """Masked attention by the textbook formula, fp64, gradients by autograd."""
+    q = q.clone().requires_grad_(True)
+    k = k.clone().requires_grad_(True)
+    v = v.clone().requires_grad_(True)
+    s = scale * q @ k.transpose(-1, -2)
+    dead = M.all(dim=-1, keepdim=True)                 # rows with nothing attended
+    s = s.masked_fill(M, float("-inf")).masked_fill(dead, 0.0)
+    p = torch.softmax(s, dim=-1).masked_fill(dead, 0.0)
+    o = p @ v
+    lse = torch.logsumexp(s, dim=-1).masked_fill(dead.squeeze(-1), float("-inf"))
+    o.backward(dO)
+    return o.detach(), lse.detach(), q.grad, k.grad, v.grad
+
+
+@pytest.mark.parametrize("seed,N,d", [(0, 40, 16), (1, 64, 32), (2, 17, 8), (3, 50, 16)])
+def test_oracle_matches_torch_bruteforce(seed, N, d):
+    rng = np.random.default_rng(seed)
+    m = _rand_mask(N, rng)
+    if seed == 3:                      # causal plus a block of fully masked rows
+        m = dict(lts=np.full((1, 1, N), 10, np.int32), lte=np.full((1, 1, N), 14, np.int32),
+                 uts=np.zeros((1, 1, N), np.int32), ute=np.arange(N, dtype=np.int32)[None, None])
+    g = torch.Generator().manual_seed(seed)
+    q, k, v, dO = (torch.randn(1, 1, N, d, generator=g, dtype=torch.float64).to(torch.bfloat16)
+                   for _ in range(4))
+    scale = 1.0 / np.sqrt(d)
+    M = torch.from_numpy(oracle.dense_from_cols(*_bounds(m)))
+    ro, rl, rdq, rdk, rdv = _torch_reference(*(t[0, 0].double() for t in (q, k, v, dO)), M, scale)
+    O, lse = oracle.forward(q, k, v, m, scale)
+    gr = oracle.backward(q, k, v, dO, m, scale)
+    np.testing.assert_allclose(O[0, 0], ro.numpy(), atol=1e-12, rtol=1e-10)
+    fin = np.isfinite(rl.numpy())
+    assert np.array_equal(fin, np.isfinite(lse[0, 0]))
+    np.testing.assert_allclose(lse[0, 0][fin], rl.numpy()[fin], atol=1e-12, rtol=1e-10)
+    assert np.all(lse[0, 0][~fin] == -np.inf)
+    for ours, ref in ((gr["dq"], rdq), (gr["dk"], rdk), (gr["dv"], rdv)):
+        np.testing.assert_allclose(ours[0, 0], ref.numpy(), atol=1e-11, rtol=1e-9)
+    np.testing.assert_allclose(gr["lse"][0, 0][fin], rl.numpy()[fin], atol=1e-12)
+    if seed == 3:
+        assert (~fin).sum() == 4         # rows 10..13 see nothing
+
+
+def test_oracle_gradients_by_finite_differences():
+    """Central differences of L = sum(O * dO) through the oracle's forward."""
+    rng = np.random.default_rng(7)
+    N, d = 24, 8
+    m = _rand_mask(N, rng)
+    g = torch.Generator().manual_seed(7)
+    q, k, v, dO = (torch.randn(1, 1, N, d, generator=g).to(torch.bfloat16).float() for _ in range(4))
+    scale = 0.35
+    gr = oracle.backward(q, k, v, dO, m, scale)
+    h = 2.0 ** -12                     # exact in fp32 next to bf16 values
+
+    def loss(qq, kk, vv):
+        O, _ = oracle.forward(qq, kk, vv, m, scale)
+        return float((O[0, 0] * dO[0, 0].double().numpy()).sum())
+
+    for name, idx in (("dq", 0), ("dk", 1), ("dv", 2)):
+        for _ in range(8):
+            r, c = int(rng.integers(N)), int(rng.integers(d))
+            ins = [q.clone(), k.clone(), v.clone()]
+            ins[idx][0, 0, r, c] += h
+            lp = loss(*ins)
+            ins[idx][0, 0, r, c] -= 2 * h
+            lm = loss(*ins)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - gr[name][0, 0, r, c]) < 2e-5 * max(1.0, abs(fd)), (name, r, c)
+
+
+def test_invariants_constant_v_single_key_dead_rows():
+    N, d = 96, 16
+    # rows 0..9 see only column 5, rows 10..19 see nothing, the rest see a causal window.
+    lts = np.full(N, N, np.int32); lte = np.full(N, N, np.int32)
+    uts = np.zeros(N, np.int32); ute = np.arange(N, dtype=np.int32)
+    uts[:] = 0
+    ute[:] = np.maximum(np.arange(N), 20)          # rows < max(j, 20) masked ...
+    ute[5] = 0; lts[5] = 10; lte[5] = 20           # ... except column 5: rows 0..9 attend it
+    ute[N - 1] = N                                 # the last column is attended by nobody
+    m = dict(lts=lts[None, None], lte=lte[None, None], uts=uts[None, None], ute=ute[None, None])
+    M = oracle.dense_from_cols(lts, lte, uts, ute)
+    assert M[:10].sum(1).tolist() == [N - 1] * 10 and M[10:20].all()
+    g = torch.Generator().manual_seed(3)
+    q, k, dO = (torch.randn(1, 1, N, d, generator=g).to(torch.bfloat16) for _ in range(3))
+    vrow = torch.randn(d, generator=g).to(torch.bfloat16)
+    v = vrow.expand(1, 1, N, d).contiguous()
+    O, lse = oracle.forward(q, k, v, m, 0.25)
+    live = ~M.all(1)
+    np.testing.assert_allclose(O[0, 0][live], np.broadcast_to(vrow.double().numpy(), (live.sum(), d)),
+                               atol=1e-13)                          # constant V returns V
+    assert np.all(O[0, 0][~live] == 0) and np.all(lse[0, 0][~live] == -np.inf)
+    v2 = torch.randn(1, 1, N, d, generator=g).to(torch.bfloat16)
+    O2, lse2 = oracle.forward(q, k, v2, m, 0.25)
+    np.testing.assert_allclose(O2[0, 0][:10], np.broadcast_to(v2[0, 0, 5].double().numpy(), (10, d)),
+                               atol=1e-13)                          # single key returns its row
+    s5 = 0.25 * (q[0, 0, :10].double() @ k[0, 0, 5].double()).numpy()
+    np.testing.assert_allclose(lse2[0, 0][:10], s5, atol=1e-13)     # lse = that key's score
+    gr = oracle.backward(q, k, v2, dO, m, 0.25)
+    assert np.all(gr["dq"][0, 0][~live] == 0)
+    never = M.all(0)                                                 # columns nobody attends
+    assert never.any()
+    assert np.all(gr["dk"][0, 0][never] == 0) and np.all(gr["dv"][0, 0][never] == 0)
+    # D_i = dO_i . O_i
+    np.testing.assert_allclose(gr["D"][0, 0], (O2[0, 0] * dO[0, 0].double().numpy()).sum(1), atol=1e-12)
+
+
+def test_key_shift_invariance():
+    """Adding c to every key leaves P, O and dQ unchanged (sum_j dS_ij = 0) and
+    moves lse_i by scale * q_i . c."""
+    rng = np.random.default_rng(11)
+    N, d = 48, 16
+    m = _rand_mask(N, rng)
+    g = torch.Generator().manual_seed(11)
+    q, k, v, dO = (torch.randn(1, 1, N, d, generator=g).to(torch.bfloat16) for _ in range(4))
+    c = torch.full((d,), 0.5)
+    k2 = k.float() + c                 # fp32 input: the shift is exact for bf16 keys
+    assert torch.equal(k2 - c, k.float())
+    scale = 0.3
+    O, lse = oracle.forward(q, k, v, m, scale)
+    O2, lse2 = oracle.forward(q, k2, v, m, scale)
+    gr, gr2 = oracle.backward(q, k, v, dO, m, scale), oracle.backward(q, k2, v, dO, m, scale)
+    np.testing.assert_allclose(O2, O, atol=1e-12)
+    np.testing.assert_allclose(gr2["dq"], gr["dq"], atol=1e-11)
+    fin = np.isfinite(lse)
+    shift = scale * (q[0, 0].double() @ c.double()).numpy()
+    np.testing.assert_allclose((lse2 - lse)[fin], np.broadcast_to(shift, lse.shape)[fin], atol=1e-11)
+
+
+def test_row_and_column_forms_give_the_same_dense_mask():
+    for wl in list(W.SMALL.values()) + [W.FULL["tiny_causal"], W.FULL["doc_packing"].with_(B=1)]:
+        m = _mask_np(wl)
+        if m["rows"] is None:
+            continue
+        for b in range(wl.B):
+            for hm in range(wl.Hm):
+                Mr = oracle.dense_from_rows(m["rows"][0][b, hm], m["rows"][1][b, hm])
+                Mc = oracle.dense_from_cols(*_bounds(m, b, hm))
+                assert np.array_equal(Mr, Mc), (wl.name, b, hm)
+
+
+def _counts(lbl):
+    return dict(skip=int((lbl == 0).sum()), full=int((lbl == 1).sum()), partial=int((lbl == 2).sum()))
+
+
+def test_golden_causal_example():
+    gd = json.load(open(os.path.join(GOLDEN, "causal_row_form.json")))
+    N = gd["N"]
+    Mr = oracle.dense_from_rows(gd["col_start"], gd["col_end"])
+    e = gd["expect_columns"]
+    Mc = oracle.dense_from_cols(e["lts"], e["lte"], e["uts"], e["ute"])
+    assert np.array_equal(Mr, Mc) and Mr.shape == (N, N)
+    for tc in gd["tile_counts"]:
+        wl = W.Workload("c", 1, 1, tc["N"], 64, "causal")
+        m = _mask_np(wl)
+        got = _counts(oracle.tile_labels(*_bounds(m), tc["bq"], tc["bk"]))
+        assert got == {k: tc[k] for k in ("skip", "full", "partial")}, tc
+        if tc["N"] <= 4096:
+            exact = _counts(oracle.tile_labels(*_bounds(m), tc["bq"], tc["bk"], exact=True))
+            assert exact == got
+    wl = W.Workload("c", 1, 1, gd["attended_pairs"]["N"], 64, "causal")
+    assert oracle.attended_pairs(*_bounds(_mask_np(wl))) == gd["attended_pairs"]["pairs"]
+
+
+def test_golden_doc_packing_example():
+    gd = json.load(open(os.path.join(GOLDEN, "doc_packing_example.json")))
+    N = gd["N"]
+    # The page's construction: rows of a document at offset o get (o, o + i).
+    cs, ce, off = [], [], 0
+    for L in gd["doc_lengths"]:
+        for i in range(L):
+            cs.append(off); ce.append(off + i)
+        off += L
+    assert off == N
+    for row, a, b in gd["row_spot_checks"]:
+        assert (cs[row], ce[row]) == (a, b)
+    # Independent column form: the generator's document-packing bounds.
+    wl = W.Workload("docs", 1, 1, N, 128, "docs_uniform")
+    docs = [gd["doc_lengths"]]
+    cols = W._one_mask(wl, 0, 0, docs, None)[0]
+    Mr = oracle.dense_from_rows(cs, ce)
+    assert np.array_equal(Mr, oracle.dense_from_cols(*cols))
+    assert int((~Mr).sum()) == gd["attended_pairs"] == oracle.attended_pairs(*cols)
+    lbl = oracle.tile_labels(*cols, 128, 128)
+    assert _counts(lbl) == {k: gd["tile_counts_128"][k] for k in ("skip", "full", "partial")}
+    assert np.array_equal(lbl, oracle.tile_labels(*cols, 128, 128, exact=True))
+    sm = gd["small"]
+    e = sm["expect_columns"]
+    assert np.array_equal(oracle.dense_from_rows(sm["col_start"], sm["col_end"]),
+                          oracle.dense_from_cols(e["lts"], e["lte"], e["uts"], e["ute"]))
+
+
+@pytest.mark.parametrize("name,pairs", [
+    ("tiny_causal", 32896),
+    ("sliding_window", 33030656),        # sum_i min(i + 1, 1024)
+    ("prefix_lm", 142612480),            # 4096^2 + sum_{i=4096}^{16383} (i + 1)
+])
+def test_attended_pairs_closed_form(name, pairs):
+    wl = W.FULL[name]
+    m = _mask_np(wl)
+    assert oracle.attended_pairs(*_bounds(m)) == pairs
+    N = wl.N
+    if name == "sliding_window":
+        assert pairs == sum(min(i + 1, 1024) for i in range(N))
+    if name == "prefix_lm":
+        assert pairs == 4096 ** 2 + sum(i + 1 for i in range(4096, N))
+
+
+def test_attended_pairs_docs_closed_form():
+    for wl in (W.FULL["doc_packing"], W.SMALL["docs_small"], W.SMALL["lognormal_small"]):
+        m = _mask_np(wl)
+        for b in range(wl.B):
+            want = sum(L * (L + 1) // 2 for L in m["docs"][b])
+            assert oracle.attended_pairs(*_bounds(m, b)) == want
+            assert sum(m["docs"][b]) == wl.N
+
+
+@pytest.mark.parametrize("name", ["tiny_causal", "doc_packing", "sliding_window", "prefix_lm",
+                                  "causal_ragged", "docs_small", "window_small", "prefix_small",
+                                  "lognormal_small", "unmasked_small", "all_masked_small"])
+@pytest.mark.parametrize("bq,bk", [(128, 128), (64, 128), (64, 64), (128, 64)])
+def test_labels_equal_exact_on_structured_masks(name, bq, bk):
+    wl = W.FULL.get(name) or W.SMALL[name]
+    m = _mask_np(wl)
+    for b in range(wl.B):
+        lbl = oracle.tile_labels(*_bounds(m, b), bq, bk)
+        ex = oracle.tile_labels(*_bounds(m, b), bq, bk, exact=True)
+        assert np.array_equal(lbl, ex), (name, b)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_labels_sound_on_arbitrary_bounds(seed):
+    rng = np.random.default_rng(100 + seed)
+    N = int(rng.integers(1, 700))
+    m = _rand_mask(N, rng)
+    for bq, bk in ((128, 128), (64, 128), (64, 64)):
+        lbl = oracle.tile_labels(*_bounds(m), bq, bk)
+        ex = oracle.tile_labels(*_bounds(m), bq, bk, exact=True)
+        assert np.all(ex[lbl == 0] == 0)          # SKIP only where all is masked
+        assert np.all(ex[lbl == 1] == 1)          # FULL only where nothing is masked
+        assert np.all(lbl[ex == 0] != 1) and np.all(lbl[ex == 1] != 0)
+
+
+def test_labels_sound_on_prefix_random():
+    wl = W.FULL["prefix_random"]
+    m = _mask_np(wl)
+    lbl = oracle.tile_labels(*_bounds(m))
+    ex = oracle.tile_labels(*_bounds(m), exact=True)
+    assert np.all(ex[lbl == 0] == 0) and np.all(ex[lbl == 1] == 1)
+    assert (lbl == 2).sum() > (lbl == 1).sum()    # the stress case is mostly partial tiles
+
+
+def test_softmax_max_subtraction_identity():
+    """FlashAttention article §二.2: subtracting the row max leaves softmax unchanged;
+    the oracle's stabilised lse equals the naive log-sum-exp where that is finite."""
+    rng = np.random.default_rng(5)
+    N, d = 32, 8
+    m = dict(lts=np.full((1, 1, N), N, np.int32), lte=np.full((1, 1, N), N, np.int32),
+             uts=np.zeros((1, 1, N), np.int32), ute=np.arange(N, dtype=np.int32)[None, None])
+    g = torch.Generator().manual_seed(5)
+    q, k, v = (torch.randn(1, 1, N, d, generator=g).to(torch.bfloat16) for _ in range(3))
+    _, lse = oracle.forward(q, k, v, m, 0.5)
+    s = 0.5 * (q[0, 0].double() @ k[0, 0].double().T).numpy()
+    naive = np.log(np.array([np.exp(s[i, : i + 1]).sum() for i in range(N)]))
+    np.testing.assert_allclose(lse[0, 0], naive, rtol=1e-13)
