@@ -1,0 +1,343 @@
+"""Benchmark: FlashMask-style masked attention, forward + backward, on the
+128K long-context document-packing workload (B=1, H=8, N=131072, d=128,
+log-normal documents, causal within each document).
+
+One step = one pass of the hot path over the workload: tile classification,
+forward, backward (preprocess, main, dQ postprocess).  The metric is TFLOP/s
+on unmasked FLOPs (4d per attended (i, j) pair per head forward, 10d
+backward, 14d together); `value` is the fwd+bwd figure with inputs resident
+in HBM.  `e2e` repeats the step through the C ABI from pinned host buffers:
+row-form mask conversion on the host, host-to-device copies of Q, K, V, dO
+and the bounds, the device work, and device-to-host copies of O, lse, dQ,
+dK, dV, all inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fm|reference]
+Under torchrun every rank runs the whole workload on its own GPU (independent
+replicas, weak scaling); time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from long_context_fm_gb300 import workloads as W  # noqa: E402
+
+METRIC = "fwd and fwd+bwd TFLOP/s on unmasked FLOPs (% of GB300 BF16 peak) at N=128K"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
+# the hash of the kernel source it was taken on (stale entries are ignored).
+NCU_TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_hash(name):
+    path = os.path.join(ROOT, "long_context_fm_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (path, os.path.join(ROOT, "long_context_fm_gb300", "csrc", "fm_ptx.cuh")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def attended_pairs_per_head(m, b, hm, N):
+    """Attended pairs of one mask head, from interval arithmetic on the bounds."""
+    l0, l1 = m["lts"][b, hm].astype(np.int64), m["lte"][b, hm].astype(np.int64)
+    u0, u1 = m["uts"][b, hm].astype(np.int64), m["ute"][b, hm].astype(np.int64)
+    ln, un = np.maximum(l1 - l0, 0), np.maximum(u1 - u0, 0)
+    inter = np.where((ln > 0) & (un > 0), np.maximum(np.minimum(l1, u1) - np.maximum(l0, u0), 0), 0)
+    return int((N - (ln + un - inter)).sum())
+
+
+def total_pairs(wl, m):
+    tot = 0
+    for b in range(wl.B):
+        for h in range(wl.H):
+            tot += attended_pairs_per_head(m, b, h if wl.Hm == wl.H else 0, wl.N)
+    return tot
+
+
+def run_fm(args, rank, world, local_rank):
+    from long_context_fm_gb300 import fm
+
+    wl = W.FULL[args.config]
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    m = W.make_mask(wl)
+    pairs = total_pairs(wl, m)
+    d = wl.d
+    fwd_flops = 4.0 * d * pairs
+    bwd_flops = 10.0 * d * pairs
+    # inputs on the device (values drawn on the device, seeded per rank)
+    q, k, v, dO = W.make_inputs(wl, seed=1000 + rank, device=dev)
+    B, H, N = wl.B, wl.H, wl.N
+    stream = torch.cuda.current_stream(dev)
+    bnd = [torch.from_numpy(np.ascontiguousarray(m[x])).to(dev) for x in ("lts", "lte", "uts", "ute")]
+    bounds = fm.make_bounds(*bnd)
+    plan = torch.empty(fm.fm_plan_bytes(B, wl.Hm, N), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3))
+    ws = torch.empty(fm.fm_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    scale = wl.scale
+
+    def step():
+        fm.fm_tile_classify(bounds, plan, status, stream=stream)
+        fm.fm_attn_fwd(q, k, v, bounds, plan, scale, o, lse, status, stream=stream)
+        fm.fm_attn_bwd(q, k, v, o, lse, dO, bounds, plan, scale, dq, dk, dv, ws, status, stream=stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}: {fm.fm_status_string(int(status.item()))}")
+
+    # ---- device-resident timed region
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    fm.fm_profile_begin()
+    with ClockSampler(local_rank) as clocks:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    recs = fm.fm_profile_end()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_step = ms_total / args.steps
+    per_kernel = {}
+    for name, ms in recs:
+        per_kernel.setdefault(name, []).append(ms)
+    avg = {kname: sum(v_) / len(v_) for kname, v_ in per_kernel.items()}
+    launches = len(recs)
+
+    # ---- end to end through the C ABI from pinned host buffers
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dO))
+    rows = m["rows"]
+    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+    hdq, hdk, hdv = (torch.empty_like(dq, device="cpu").pin_memory() for _ in range(3))
+    hb = [torch.empty(bnd[0].shape, dtype=torch.int32).pin_memory() for _ in range(4)]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * hb[0].numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
+
+    def e2e_step():
+        if rows is not None:                                     # host conversion of the row form
+            cols = fm.fm_mask_from_rows(*rows)
+        else:
+            cols = [m[x] for x in ("lts", "lte", "uts", "ute")]
+        for dst, src in zip(hb, cols):
+            dst.numpy()[...] = src
+        for dst, src in zip(bnd, hb):
+            dst.copy_(src, non_blocking=True)
+        for dst, src in zip((q, k, v, dO), (hq, hk, hv, hdo)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip((ho, hl, hdq, hdk, hdv), (o, lse, dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    e2e_steps = max(1, min(args.steps, 5))
+    for _ in range(e2e_steps):
+        e2e_step()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+
+    # max over ranks
+    t = torch.tensor([ms_step, e2e_s], dtype=torch.float64)
+    if world > 1:
+        t = t.to(dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t = t.cpu()
+    ms_step, e2e_s = float(t[0]), float(t[1])
+    return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
+                avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h)
+
+
+def cpu_baseline_sample(wl, m, max_docs=3):
+    """The oracle, as it stands, on the first documents of head 0 (an
+    independent sub-problem of the same workload: causal within each
+    document, nothing across documents)."""
+    import oracle
+
+    docs = m["docs"][0]
+    S = int(sum(docs[:max_docs]))
+    sub = {x: np.minimum(m[x][:1, :1, :S], S).astype(np.int32) for x in ("lts", "lte", "uts", "ute")}
+    g = torch.Generator().manual_seed(0)
+    q, k, v, dO = (torch.randn(1, 1, S, wl.d, generator=g).to(torch.bfloat16) for _ in range(4))
+    pairs = sum(L * (L + 1) // 2 for L in docs[:max_docs])
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, sub, wl.scale)
+    oracle.backward(q, k, v, dO, sub, wl.scale)
+    dt = time.perf_counter() - t0
+    tflops = 14.0 * wl.d * pairs / dt / 1e12
+    return dict(value=tflops, unit="TFLOP/s", cores=oracle.num_threads(), kind="oracle",
+                sample=f"fp64 oracle fwd+bwd on the first {max_docs} documents of head 0 "
+                       f"({S} rows, {pairs} attended pairs), {dt:.1f} s")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fm", choices=["fm", "reference"])
+    ap.add_argument("--config", default="long_packing_128k", choices=list(W.FULL))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = W.FULL[args.config]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        m = W.make_mask(wl)
+        for _ in range(args.warmup):
+            cpu_baseline_sample(wl, m, max_docs=1)
+        vals = [cpu_baseline_sample(wl, m, max_docs=1) for _ in range(args.steps)]
+        cb = vals[-1]
+        val = statistics.median(v_["value"] for v_ in vals)
+        line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "impl": "reference",
+                "config": {"workload": wl.name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
+                           "sample": "first document of head 0 per step"},
+                "cpu_baseline": {k_: cb[k_] for k_ in ("kind", "cores", "sample")} | {"value": val, "unit": "TFLOP/s"},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    r = run_fm(args, rank, world, local_rank)
+    if rank == 0:
+        peaks, src = load_peaks()
+        fwd_ms = r["avg"].get("fwd", float("nan"))
+        bwd_ms = r["avg"].get("bwd", float("nan"))
+        step_flops = r["fwd_flops"] + r["bwd_flops"]
+        value = world * step_flops / (r["ms_step"] * 1e-3) / 1e12
+        fwd_tflops = r["fwd_flops"] / (fwd_ms * 1e-3) / 1e12
+        bwd_tflops = r["bwd_flops"] / (bwd_ms * 1e-3) / 1e12
+        peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        key = src_hash("fm_bwd.cu")
+        traffic = NCU_TRAFFIC.get(("bwd", key))
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": r["wl"].name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
+                       "mask": "log-normal documents (median 4096, sigma 1, clip [256, 32768]), causal within document",
+                       "attended_pairs": r["pairs"], "outputs": "fp32 O, dQ, dK, dV",
+                       "l2": "inputs larger than L2 (Q, K, V, dO 1 GiB), no flush"},
+            "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+            "frac_of_peak": {"fwd": fwd_tflops / peak_burst, "fwd_bwd": value / world / peak_sus,
+                             "peaks": f"{src}: bf16 burst {peak_burst}, sustained {peak_sus}"},
+            "kernel_ms": r["avg"],
+            "roofline": {"kernel": "fm_bwd_kernel", "bound": "tensor", "achieved": bwd_tflops,
+                         "peak": peak_sus, "unit": "TFLOP/s", "frac": bwd_tflops / peak_sus,
+                         "traffic": traffic, "peak_source": f"{src} bf16 sustained"},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+            "e2e": {"value": world * step_flops / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline_sample(wl, W.make_mask(wl), max_docs=1)
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * fm.h — C ABI of the GB300 (sm_103a) FlashMask-style masked attention library.
+ *
+ * The method (FlashMask, arXiv 2410.01359, abstract): attention masks are
+ * carried as O(N) column-wise bounds instead of a dense N x N matrix, and the
+ * kernels use them to skip (Q-tile, KV-tile) blocks that are fully masked,
+ * run fully visible blocks without any mask arithmetic, and apply the
+ * per-element mask only on the remaining boundary blocks (blog post
+ * "FlashMask技术", §2.2, three-way block decision).  The result is plain
+ * masked softmax attention, exactly (blog §2.2, "mathematically
+ * equivalent"; abstract, "without sacrificing computational accuracy").
+ *
+ * Mask encoding used throughout: for batch b, mask head hm and key column j,
+ *     lower masked rows [lts_j, lte_j)   and   upper masked rows [uts_j, ute_j)
+ * (half-open; start >= end is an empty range; all values in [0, N]).
+ * Element (i, j) is masked when query row i lies in either range.  The
+ * arrays are int32 [B, Hm, N], row-major; Hm is 1 (one mask for all heads)
+ * or H (one mask per head).  Head h reads mask head (Hm == 1 ? 0 : h).
+ *
+ * Tensors: Q, K, V, dO are bf16 [B, H, N, d] contiguous (d = 64 or 128);
+ * lse is fp32 [B, H, N] (natural log); outputs are bf16 or fp32 [B, H, N, d].
+ *
+ * Conventions
+ *  - Memory: every buffer is allocated by the caller.  The library allocates
+ *    no device memory and keeps no pointer after a call returns.
+ *  - Device calls are asynchronous on the given stream (NULL = legacy
+ *    default stream).  Argument errors are returned before anything is
+ *    launched.  Errors the device detects (a bound outside [0, N], a plan
+ *    that does not match the call, a pipeline wait that ran out) are written
+ *    to the caller's int32 dev_status (zero it first; the first error wins)
+ *    and read by the caller after synchronising.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Thread safety: calls may be made from several host threads.
+ */
+#ifndef FM_H_
+#define FM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FM_API __attribute__((visibility("default")))
+#else
+#define FM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FM_OK = 0,
+    FM_ERR_INVALID_ARG = 1,      /* null / misaligned pointer, bad size or dtype          */
+    FM_ERR_UNSUPPORTED = 2,      /* head dim, tile size or device not supported          */
+    FM_ERR_UNREPRESENTABLE = 3,  /* row-form mask with > 2 masked ranges in some column  */
+    FM_ERR_BAD_BOUNDS = 4,       /* a bound outside [0, N] (host or device detected)     */
+    FM_ERR_PLAN_MISMATCH = 5,    /* plan built for other shapes or tile sizes            */
+    FM_ERR_WORKSPACE = 6,        /* workspace missing or too small                       */
+    FM_ERR_CUDA = 7,             /* a CUDA runtime / driver call failed                  */
+    FM_ERR_TIMEOUT = 8           /* a bounded device-side wait ran out (kernel returned) */
+} fm_status;
+
+enum { FM_TILE_SKIP = 0, FM_TILE_FULL = 1, FM_TILE_PARTIAL = 2 };
+enum { FM_DT_BF16 = 0, FM_DT_F32 = 1 };
+
+/* Same type as cudaStream_t, so a cudaStream_t can be passed directly. */
+typedef struct CUstream_st *fm_stream_t;
+
+/* Column-bound mask; the four pointers are DEVICE arrays int32 [B, Hm, N]. */
+typedef struct {
+    const int32_t *lts, *lte, *uts, *ute;
+    int32_t B, Hm, N;
+} fm_bounds;
+
+/* Human-readable name of a status code (static storage). */
+FM_API const char *fm_status_string(fm_status st);
+
+/* Library ABI version (incremented when a signature changes). */
+FM_API int fm_abi_version(void);
+
+/*
+ * fm_mask_from_rows — HOST, synchronous.
+ * Passage: blog "FlashMask技术" §2.1 (causal example) and §3.3 (document
+ * packing): one inclusive attend interval [cs_i, ce_i] per query row.
+ * cs, ce: host int32 [B, Hm, N]; cs_i > ce_i is an empty row; otherwise
+ * 0 <= cs_i <= ce_i < N is required (else FM_ERR_BAD_BOUNDS).
+ * Writes the column form to host arrays lts, lte, uts, ute [B, Hm, N]:
+ * for each column the rows that do NOT attend it must form at most two
+ * ranges (else FM_ERR_UNREPRESENTABLE, outputs then undefined).  A masked
+ * range that starts at row 0 is stored as the upper range, any other (or the
+ * second of two) as the lower range; empty ranges are written canonically,
+ * lower (N, N) and upper (0, 0).  Runs in O(N) per (b, hm).
+ */
+FM_API fm_status fm_mask_from_rows(const int32_t *cs, const int32_t *ce, int B, int Hm, int N,
+                            int32_t *lts, int32_t *lte, int32_t *uts, int32_t *ute);
+
+/*
+ * Plan = tile labels plus, per Q tile, the ordered list of non-skip KV tiles
+ * and, per KV tile, the list of non-skip Q tiles (blog §4.1 item 2: decide
+ * before a KV block is loaded whether it is needed at all).  Opaque device
+ * buffer of fm_plan_bytes() bytes, 256-byte aligned, written by
+ * fm_tile_classify and read by fm_attn_fwd / fm_attn_bwd.
+ * bq, bk in {64, 128}; the attention kernels need bq = bk = 128.
+ * Returns 0 for invalid sizes.
+ */
+FM_API size_t fm_plan_bytes(int B, int Hm, int N, int bq, int bk);
+
+/*
+ * fm_tile_classify — DEVICE, async.
+ * Passage: blog §2.2 (skip / full GEMM / masked GEMM per block pair).  The
+ * printed test is garbled; the decision implemented is: per KV tile take the
+ * min and max of each canonicalised bound (empty lower -> (N, N), empty
+ * upper -> (0, 0)) over its columns; for Q rows [qb, qe) the pair is
+ *   SKIP    if all columns' lower ranges cover [qb, qe) or all upper ones do,
+ *   FULL    if not SKIP and every lower and every upper range misses [qb, qe),
+ *   PARTIAL otherwise (tile ends clipped to N).
+ * labels (nullable): device uint8 [B, Hm, n_q, n_k] copy of the labels.
+ * dev_status: device int32 (required).  Bounds outside [0, N] set
+ * FM_ERR_BAD_BOUNDS there.
+ */
+FM_API fm_status fm_tile_classify(fm_bounds m, int bq, int bk, void *plan, size_t plan_bytes,
+                           uint8_t *labels, int32_t *dev_status, fm_stream_t stream);
+
+/* Workspace of fm_attn_fwd in bytes (may be 0: then ws may be NULL). */
+FM_API size_t fm_fwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fm_attn_fwd — DEVICE, async.
+ * Passages: FlashAttention article §二.1-二.3 (tiling, max-subtracted
+ * softmax, QK^T and PV fused on tensor cores), blog §2.2 and §4.1 items 2-3
+ * (skip blocks before loading them, mask fused into the softmax on boundary
+ * blocks only).  Computes, per (b, h),
+ *     O = softmax(scale * Q K^T with masked entries removed) V,
+ *     lse_i = ln sum_{j attended} exp(scale q_i.k_j)
+ * with O_i = 0 and lse_i = -inf for a row that attends nothing.
+ * q, k, v: device bf16 [B, H, N, d]; plan from fm_tile_classify(m, 128, 128);
+ * o: device [B, H, N, d] of o_dtype (FM_DT_BF16 / FM_DT_F32);
+ * lse: device fp32 [B, H, N]; ws: fm_fwd_workspace_bytes() bytes or NULL.
+ */
+FM_API fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, const void *plan,
+                      int B, int H, int N, int d, float scale, void *o, int o_dtype, float *lse,
+                      void *ws, size_t ws_bytes, int32_t *dev_status, fm_stream_t stream);
+
+/* Workspace of fm_attn_bwd in bytes: fp32 dQ accumulator [B,H,N,d] plus
+ * fp32 D = rowsum(dO * O) [B,H,N]. */
+FM_API size_t fm_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * fm_attn_bwd — DEVICE, async.
+ * Exact gradient of fm_attn_fwd's O with upstream dO (lse has no upstream
+ * gradient); the pages use the method for training (abstract: SFT, LoRA,
+ * DPO, RM), which needs these.  With P_ij = exp(scale q_i.k_j - lse_i) on
+ * attended pairs (0 elsewhere), D_i = sum_k dO_ik O_ik:
+ *     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q.
+ * Same tile skipping as the forward.  o, lse: the forward's outputs (o of
+ * o_dtype); dq, dk, dv: device [B, H, N, d] of grad_dtype; ws:
+ * fm_bwd_workspace_bytes() bytes (overwritten).
+ */
+FM_API fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o, int o_dtype,
+                      const float *lse, const void *dO, fm_bounds m, const void *plan, int B,
+                      int H, int N, int d, float scale, void *dq, void *dk, void *dv,
+                      int grad_dtype, void *ws, size_t ws_bytes, int32_t *dev_status,
+                      fm_stream_t stream);
+
+/*
+ * Per-kernel timing (the library's own tracing).  fm_profile_begin starts
+ * recording a CUDA event pair around every kernel the library launches
+ * (process-wide, up to 4096 launches); fm_profile_end waits for those
+ * events, writes up to max_entries (kernel id, milliseconds) records and
+ * stops recording.  Returns the number of records written, or -1 on error.
+ */
+enum { FM_K_CLASSIFY_MINMAX = 0, FM_K_CLASSIFY_LISTS = 1, FM_K_FWD = 2, FM_K_BWD_PRE = 3,
+       FM_K_BWD = 4, FM_K_BWD_POST = 5, FM_K_COUNT = 6 };
+typedef struct {
+    int32_t kernel;
+    float ms;
+} fm_kernel_time;
+FM_API fm_status fm_profile_begin(void);
+FM_API int fm_profile_end(fm_kernel_time *out, int max_entries);
+
+/*
+ * Self-test of the bounded wait used by every pipeline barrier: one CTA
+ * waits on a barrier that nothing completes, gives up after about
+ * limit_cycles SM clock cycles and writes FM_ERR_TIMEOUT to dev_status.
+ * Lets failure detection be tested without hanging a GPU.
+ */
+FM_API fm_status fm_selftest_wait_timeout(long long limit_cycles, int32_t *dev_status,
+                                   fm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FM_H_ */

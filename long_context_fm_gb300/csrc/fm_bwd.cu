@@ -1,0 +1,516 @@
+// Backward masked attention on sm_103a: preprocess, main kernel, dQ
+// postprocess.
+//
+// The gradients are those of plain masked softmax attention (the method is
+// exact: blog "FlashMask技术" §2.2, arXiv 2410.01359 abstract), with the
+// same tile skipping as the forward (blog §2.2): fully masked (Q tile, KV
+// tile) pairs are never visited, fully visible pairs run without mask
+// arithmetic, only partial pairs evaluate the column-interval predicate.
+//
+// Main kernel: one CTA = one (b, h, 128-row KV tile); it walks the plan's
+// list of non-skip Q tiles of that KV tile, each as two 64-row halves.
+//   warp 0      TMA producer (K and V once; Q, dO halves double-buffered;
+//               lse and D staged into shared memory by the whole warp)
+//   warp 1      TMEM allocation; one thread issues the tcgen05 MMAs
+//   warps 2-5   one thread per KV row j: P^T and dS^T for the half
+//   warps 6-9   one thread per head-dim index: drains dQ^T from TMEM and adds
+//               it into the fp32 dQ accumulator (coalesced red.global.add)
+// TMEM (512 columns): dK [0, d), dV [128, 128 + d), S^T [256, 320),
+// dP^T [320, 384), dQ^T [384, 448).  Per half (M = 128 KV rows):
+//   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
+//   dP^T = V dO^T       (SS, K-major/K-major)        -> TMEM
+//   P^T  = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T o (dP^T - D)
+//          written as bf16 into 128-byte-swizzled shared memory
+//   dV  += P^T dO       (SS, P^T K-major, dO MN-major)
+//   dK  += dS^T Q       (SS, dS^T K-major, Q MN-major)
+//   dQ^T = K^T dS^T     (SS, K MN-major, dS^T MN-major)
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fm_internal.h"
+#include "fm_ptx.cuh"
+
+namespace fm {
+
+// ---------------------------------------------------------------- preprocess
+// D[row] = sum_k dO[row, k] * O[row, k]; dQacc[row, :] = 0.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) fm_bwd_pre_kernel(const void *o, int o_f32, const uint16_t *dO,
+                                                         float *Dout, float *dq_acc, int64_t rows)
+{
+    constexpr int PER = D / 32;   // elements per lane: 4 or 2
+    const int lane = threadIdx.x & 31;
+    int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t stride = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (; row < rows; row += stride) {
+        const int64_t base = row * D + lane * PER;
+        float ov[PER], dv[PER];
+        if (o_f32) {
+            const float *op = reinterpret_cast<const float *>(o) + base;
+            if constexpr (PER == 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(op);
+                ov[0] = x.x; ov[1] = x.y; ov[2] = x.z; ov[3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2 *>(op);
+                ov[0] = x.x; ov[1] = x.y;
+            }
+        } else {
+            const uint16_t *op = reinterpret_cast<const uint16_t *>(o) + base;
+#pragma unroll
+            for (int u = 0; u < PER; ++u) ov[u] = __uint_as_float((uint32_t)op[u] << 16);
+        }
+#pragma unroll
+        for (int u = 0; u < PER; ++u) dv[u] = __uint_as_float((uint32_t)dO[base + u] << 16);
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) acc = fmaf(ov[u], dv[u], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) Dout[row] = acc;
+        float *z = dq_acc + base;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) z[u] = 0.f;
+    }
+}
+
+// ---------------------------------------------------------------- postprocess
+// dQ = scale * dQacc, converted to the gradient dtype.  4 elements per thread.
+__global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, void *dq, int g_f32,
+                                                          float scale, int64_t n4)
+{
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        const float4 x = reinterpret_cast<const float4 *>(dq_acc)[t];
+        if (g_f32) {
+            reinterpret_cast<float4 *>(dq)[t] = make_float4(x.x * scale, x.y * scale, x.z * scale, x.w * scale);
+        } else {
+            uint2 w;
+            w.x = pack_bf16x2(x.x * scale, x.y * scale);
+            w.y = pack_bf16x2(x.z * scale, x.w * scale);
+            reinterpret_cast<uint2 *>(dq)[t] = w;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- main kernel
+template <int D>
+struct BwdSmem {
+    static constexpr int kKBox = 128 * 128;     // 64 columns x 128 rows
+    static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
+    static constexpr int kKTile = 128 * D * 2;
+    static constexpr int kQTile = 64 * D * 2;
+    static constexpr int kK = 0, kV = kKTile;
+    static constexpr int kQ = 2 * kKTile;                 // [2] stages
+    static constexpr int kdO = kQ + 2 * kQTile;           // [2] stages
+    static constexpr int kP = kdO + 2 * kQTile;           // 128 x 64 bf16
+    static constexpr int kdS = kP + 128 * 128;
+    static constexpr int kStat = kdS + 128 * 128;         // lse2 [2][64], D [2][64]
+    static constexpr int kBar = kStat + 4 * 64 * 4;
+    static constexpr int kNumBar = 16;
+    static constexpr int kMisc = kBar + kNumBar * 8;
+    // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
+    static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
+};
+
+enum {
+    BB_KV = 0, BB_QF0, BB_QF1, BB_QE0, BB_QE1, BB_SF, BB_SE, BB_PF, BB_DSE, BB_DQF, BB_DQE, BB_ACC,
+    BB_DRAIN
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fm_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdArgs a)
+{
+    using S = BwdSmem<D>;
+    constexpr int NBOX = D / 64;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
+    uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
+    uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS;
+    float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [2][64]
+    float *sD = sLse + 128;                                          // [2][64]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kMisc);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
+    int *cnt_sh = reinterpret_cast<int *>(smem + S::kMisc + 8);
+    int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
+
+    const int warp = warp_id(), lane = lane_id();
+    const PlanLayout &L = a.L;
+    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
+    const int bh = b * a.H + h;
+    const int N = a.N;
+    const int kb = kt * 128;
+
+    if (threadIdx.x == 0) {
+        const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(a.plan);
+        const bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
+                        ph->bq == 128 && ph->bk == 128;
+        if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
+        *ok_sh = ok;
+        *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)sidx * L.n_k + kt] : 0;
+        *abort = 0;
+        mbar_init(&bars[BB_KV], 1);
+        mbar_init(&bars[BB_QF0], 32);
+        mbar_init(&bars[BB_QF1], 32);
+        mbar_init(&bars[BB_QE0], 1);
+        mbar_init(&bars[BB_QE1], 1);
+        mbar_init(&bars[BB_SF], 1);
+        mbar_init(&bars[BB_SE], 128);
+        mbar_init(&bars[BB_PF], 128);
+        mbar_init(&bars[BB_DSE], 1);
+        mbar_init(&bars[BB_DQF], 1);
+        mbar_init(&bars[BB_DQE], 128);
+        mbar_init(&bars[BB_ACC], 1);
+        mbar_init(&bars[BB_DRAIN], 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t tdK = tmem, tdV = tmem + 128, tS = tmem + 256, tdP = tmem + 320, tdQ = tmem + 384;
+    const int cnt = *cnt_sh;
+    const int32_t *list =
+        reinterpret_cast<const int32_t *>(a.plan + L.off_col_list) + ((int64_t)sidx * L.n_k + kt) * L.n_q;
+
+    if (*ok_sh) {
+        if (warp == 0) {
+            // ------------------------------------------------ producer
+            if (lane == 0) {
+                tma_prefetch_desc(&tq); tma_prefetch_desc(&tk);
+                tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
+                if (cnt > 0) {
+                    mbar_arrive_expect_tx(&bars[BB_KV], 2 * S::kKTile);
+#pragma unroll
+                    for (int x = 0; x < NBOX; ++x) {
+                        tma_load_3d(sK + x * S::kKBox, &tk, &bars[BB_KV], x * 64, kb, bh);
+                        tma_load_3d(sV + x * S::kKBox, &tv, &bars[BB_KV], x * 64, kb, bh);
+                    }
+                }
+            }
+            int it = 0;
+            bool ok = true;
+            for (int t = 0; t < cnt && ok; ++t) {
+                const int qtile = list[t] & kTileMask;
+                for (int half = 0; half < 2; ++half) {
+                    const int q0 = qtile * 128 + half * 64;
+                    if (q0 >= N) continue;
+                    const int st = it & 1;
+                    if (it >= 2 && !warp_wait(&bars[BB_QE0 + st], ((it >> 1) - 1) & 1, abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int r = lane + rr * 32, qi = q0 + r;
+                        float l2 = INFINITY, dd = 0.f;
+                        if (qi < N) {
+                            const float lv = a.lse[(int64_t)bh * N + qi];
+                            l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
+                            dd = a.Dvec[(int64_t)bh * N + qi];
+                        }
+                        sLse[st * 64 + r] = l2;
+                        sD[st * 64 + r] = dd;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
+#pragma unroll
+                        for (int x = 0; x < NBOX; ++x) {
+                            tma_load_3d(sQ + st * S::kQTile + x * S::kQBox, &tq, &bars[BB_QF0 + st], x * 64, q0, bh);
+                            tma_load_3d(sdO + st * S::kQTile + x * S::kQBox, &tdo, &bars[BB_QF0 + st], x * 64, q0, bh);
+                        }
+                    } else {
+                        mbar_arrive(&bars[BB_QF0 + st]);
+                    }
+                    ++it;
+                }
+            }
+            // Drain copies still in flight (only possible after an abort).
+            if (lane == 0 && *abort) {
+                if (cnt > 0) mbar_wait_drain(&bars[BB_KV], 0, a.status);
+                for (int k2 = (it > 2 ? it - 2 : 0); k2 < it; ++k2)
+                    mbar_wait_drain(&bars[BB_QF0 + (k2 & 1)], (k2 >> 1) & 1, a.status);
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+                constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
+                constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
+                const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), adS = smem_u32(sdS);
+                bool ok = cnt > 0 && mbar_wait(&bars[BB_KV], 0, abort, a.status);
+                int it = 0;
+                for (int t = 0; t < cnt && ok; ++t) {
+                    const int qtile = list[t] & kTileMask;
+                    for (int half = 0; half < 2 && ok; ++half) {
+                        const int q0 = qtile * 128 + half * 64;
+                        if (q0 >= N) continue;
+                        const int st = it & 1;
+                        const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
+                        if (!mbar_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                        if (it > 0 && !mbar_wait(&bars[BB_SE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                            mma_ss(tS, sdesc_sw128(aK + ok_, 16, 1024), sdesc_sw128(aQ + oq, 16, 1024), idS, kk > 0);
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                            mma_ss(tdP, sdesc_sw128(aV + ok_, 16, 1024), sdesc_sw128(adO + oq, 16, 1024), idS, kk > 0);
+                        }
+                        tc_commit(&bars[BB_SF]);
+                        if (!mbar_wait(&bars[BB_PF], it & 1, abort, a.status)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tdV, sdesc_sw128(aP + kk * 32, 16, 1024),
+                                   sdesc_sw128(adO + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || kk > 0));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tdK, sdesc_sw128(adS + kk * 32, 16, 1024),
+                                   sdesc_sw128(aQ + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || kk > 0));
+                        if (it > 0 && !mbar_wait(&bars[BB_DQE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ss(tdQ, sdesc_sw128(aK + kk * 2048, S::kKBox, 1024),
+                                   sdesc_sw128(adS + kk * 2048, S::kKBox, 1024), idQ, kk > 0);
+                        tc_commit(&bars[BB_DQF]);
+                        tc_commit(&bars[BB_DSE]);
+                        tc_commit(&bars[BB_QE0 + st]);
+                        ++it;
+                    }
+                }
+                if (ok && it > 0) tc_commit(&bars[BB_ACC]);
+                tc_commit(&bars[BB_DRAIN]);
+                mbar_wait_drain(&bars[BB_DRAIN], 0, a.status);
+            }
+        } else if (warp < 6) {
+            // ------------------------------------------------ P^T / dS^T
+            const int quarter = warp & 3;
+            const int r = quarter * 32 + lane;       // KV row within the tile
+            const int j = kb + r;
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            int lo0 = 0, lolen = 0, up0 = 0, uplen = 0x7fffffff;   // beyond N: masked everywhere
+            if (j < N) {
+                const int64_t o = (int64_t)sidx * N + j;
+                const int l0 = a.lts[o], l1 = a.lte[o], u0 = a.uts[o], u1 = a.ute[o];
+                lo0 = l0; lolen = max(l1 - l0, 0); up0 = u0; uplen = max(u1 - u0, 0);
+            }
+            const bool kv_tail = kb + 128 > N;
+            int it = 0;
+            bool ok = true;
+            for (int t = 0; t < cnt && ok; ++t) {
+                const int32_t e = list[t];
+                const int qtile = e & kTileMask, lab = e >> kLabelShift;
+                const bool pred = (lab == FM_TILE_PARTIAL) || kv_tail;
+                for (int half = 0; half < 2; ++half) {
+                    const int q0 = qtile * 128 + half * 64;
+                    if (q0 >= N) continue;
+                    const int st = it & 1;
+                    if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
+                        !warp_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const float *l2 = sLse + st * 64;
+                    const float *dd = sD + st * 64;
+                    // P^T row: exp2(s * scale*log2e - lse*log2e), masked -> 0.
+                    float p[64];
+                    {
+                        uint32_t raw[2][32];
+                        tmem_ld32(tS + lane_off, raw[0]);
+                        tmem_ld32(tS + lane_off + 32, raw[1]);
+                        tmem_ld_wait();
+                        tmem_reg_fence(raw[0]);
+                        tmem_reg_fence(raw[1]);
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            float pv = ex2(fmaf(__uint_as_float(raw[c >> 5][c & 31]), a.scale_log2, -l2[c]));
+                            if (pred) {
+                                const int qi = q0 + c;
+                                const bool msk = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
+                                                 ((unsigned)(qi - up0) < (unsigned)uplen);
+                                pv = msk ? 0.f : pv;
+                            }
+                            p[c] = pv;
+                        }
+                    }
+                    uint32_t draw[2][32];
+                    tmem_ld32(tdP + lane_off, draw[0]);
+                    tmem_ld32(tdP + lane_off + 32, draw[1]);
+                    tmem_ld_wait();
+                    tmem_reg_fence(draw[0]);
+                    tmem_reg_fence(draw[1]);
+                    tc_fence_before();
+                    mbar_arrive(&bars[BB_SE]);      // S^T and dP^T may now be overwritten
+                    if (it > 0 && !warp_wait(&bars[BB_DSE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                    // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
+                    uint8_t *prow = sP + r * 128;
+                    uint8_t *drow = sdS + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t pw[4], dw[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int c0 = 8 * c + 2 * u;
+                            const float ds0 = p[c0] * (__uint_as_float(draw[c0 >> 5][c0 & 31]) - dd[c0]);
+                            const float ds1 = p[c0 + 1] * (__uint_as_float(draw[(c0 + 1) >> 5][(c0 + 1) & 31]) - dd[c0 + 1]);
+                            pw[u] = pack_bf16x2(p[c0], p[c0 + 1]);
+                            dw[u] = pack_bf16x2(ds0, ds1);
+                        }
+                        const int pc = (c ^ (r & 7)) << 4;
+                        *reinterpret_cast<uint4 *>(prow + pc) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        *reinterpret_cast<uint4 *>(drow + pc) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[BB_PF]);
+                    ++it;
+                }
+            }
+            // ------------------------------------------------ dK, dV epilogue
+            if (ok && (it == 0 || warp_wait(&bars[BB_ACC], 0, abort, a.status))) {
+                tc_fence_after();
+                const bool row_in = j < N;
+                const int64_t row = (int64_t)bh * N + j;
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t tsrc = which == 0 ? tdK : tdV;
+                    const float mul = which == 0 ? a.scale : 1.f;
+                    void *dst = which == 0 ? a.dk : a.dv;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        if (it > 0) {            // warp-uniform: every lane loads
+                            tmem_ld32(tsrc + lane_off + c * 32, v);
+                            tmem_ld_wait();
+                            tmem_reg_fence(v);
+                        } else {
+#pragma unroll
+                            for (int u = 0; u < 32; ++u) v[u] = 0u;
+                        }
+                        if (!row_in) continue;
+                        if (a.g_f32) {
+                            float4 *p = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + c * 32);
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                p[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
+                                                   __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
+                        } else {
+                            uint4 *p = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + c * 32);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                p[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
+                                                  pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
+                                                  pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
+                                                  pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
+                        }
+                    }
+                }
+            }
+        } else {
+            // ------------------------------------------------ dQ drain
+            const int quarter = warp & 3;
+            const int dd = quarter * 32 + lane;      // head-dim index = TMEM lane of dQ^T
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            int it = 0;
+            bool ok = true;
+            for (int t = 0; t < cnt && ok; ++t) {
+                const int qtile = list[t] & kTileMask;
+                for (int half = 0; half < 2; ++half) {
+                    const int q0 = qtile * 128 + half * 64;
+                    if (q0 >= N) continue;
+                    if (!warp_wait(&bars[BB_DQF], it & 1, abort, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    uint32_t v[2][32];
+                    tmem_ld32(tdQ + lane_off, v[0]);
+                    tmem_ld32(tdQ + lane_off + 32, v[1]);
+                    tmem_ld_wait();
+                    tmem_reg_fence(v[0]); tmem_reg_fence(v[1]);
+                    tc_fence_before();
+                    mbar_arrive(&bars[BB_DQE]);
+                    if (dd < D) {
+                        float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
+                        const int lim = min(64, N - q0);
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
+                    }
+                    ++it;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dout, float *dq_acc,
+                            int64_t rows, int d, cudaStream_t stream)
+{
+    const int64_t warps_needed = rows;
+    int64_t blocks = (warps_needed + 7) / 8;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    ProfScope ps(kKBwdPre, stream);
+    if (d == 128)
+        fm_bwd_pre_kernel<128><<<(unsigned)blocks, 256, 0, stream>>>(o, o_f32, (const uint16_t *)dO, Dout, dq_acc, rows);
+    else
+        fm_bwd_pre_kernel<64><<<(unsigned)blocks, 256, 0, stream>>>(o, o_f32, (const uint16_t *)dO, Dout, dq_acc, rows);
+    return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &tdo, const BwdArgs &a, int d, cudaStream_t stream)
+{
+    const dim3 grid(a.L.n_k, a.H, a.B);
+    if (d == 128) {
+        constexpr int smem = BwdSmem<128>::kBytes;
+        if (cudaFuncSetAttribute(fm_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return FM_ERR_CUDA;
+        ProfScope ps(kKBwd, stream);
+        fm_bwd_kernel<128><<<grid, 320, smem, stream>>>(tq, tk, tv, tdo, a);
+    } else {
+        constexpr int smem = BwdSmem<64>::kBytes;
+        if (cudaFuncSetAttribute(fm_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return FM_ERR_CUDA;
+        ProfScope ps(kKBwd, stream);
+        fm_bwd_kernel<64><<<grid, 320, smem, stream>>>(tq, tk, tv, tdo, a);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,
+                             cudaStream_t stream)
+{
+    const int64_t n4 = n / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    ProfScope ps(kKBwdPost, stream);
+    fm_bwd_post_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, dq, g_f32, scale, n4);
+    return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}

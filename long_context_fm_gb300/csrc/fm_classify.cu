@@ -1,0 +1,171 @@
+// Tile classification (blog "FlashMask技术" §2.2: per (Q block, KV block)
+// skip / full GEMM / masked GEMM; §4.1 item 2: decide before a KV block is
+// loaded).  Two launches:
+//   1. minmax: one CTA per (b*Hm, KV tile) reduces the tile's canonicalised
+//      column bounds to 8 int32 (min and max of each bound), validates the
+//      bounds and writes the plan header;
+//   2. lists:  one CTA per (b*Hm, Q tile) writes that Q tile's label row and
+//      the ordered list of its non-skip KV tiles; one CTA per (b*Hm, KV tile)
+//      writes the list of non-skip Q tiles of that KV tile (for the
+//      KV-major backward).  Labels are recomputed from the 8 numbers, so the
+//      two halves need no other dependency.
+// HBM traffic: 16 bytes per column read, n_q*n_k label bytes and <= 8 bytes
+// per non-skip pair written.
+#include <cuda_runtime.h>
+
+#include "fm_internal.h"
+#include "fm_ptx.cuh"
+
+namespace fm {
+
+struct TileMinMax {  // canonical empty lower = (N, N), empty upper = (0, 0)
+    int32_t L0max, L0min, L1min, L1max, U0max, U0min, U1min, U1max;
+};
+
+__device__ __forceinline__ int tile_label(const TileMinMax &t, int qb, int qe)
+{
+    const bool skip = (t.L0max <= qb && t.L1min >= qe) || (t.U0max <= qb && t.U1min >= qe);
+    if (skip) return FM_TILE_SKIP;
+    const bool lower_clear = t.L0min >= qe || t.L1max <= qb;
+    const bool upper_clear = t.U0min >= qe || t.U1max <= qb;
+    return (lower_clear && upper_clear) ? FM_TILE_FULL : FM_TILE_PARTIAL;
+}
+
+__global__ void __launch_bounds__(128) classify_minmax_kernel(fm_bounds m, PlanLayout L,
+                                                              uint8_t *plan, int32_t *status)
+{
+    const int kt = blockIdx.x, s = blockIdx.y;
+    const int N = L.N, bk = L.bk;
+    const int j = kt * bk + threadIdx.x;
+    const bool in = threadIdx.x < bk && j < N;
+    int l0 = N, l1 = N, u0 = 0, u1 = 0;
+    if (in) {
+        const int64_t o = (int64_t)s * N + j;
+        l0 = m.lts[o]; l1 = m.lte[o]; u0 = m.uts[o]; u1 = m.ute[o];
+        if ((unsigned)l0 > (unsigned)N || (unsigned)l1 > (unsigned)N || (unsigned)u0 > (unsigned)N ||
+            (unsigned)u1 > (unsigned)N)
+            set_status(status, FM_ERR_BAD_BOUNDS);
+        if (l0 >= l1) { l0 = N; l1 = N; }
+        if (u0 >= u1) { u0 = 0; u1 = 0; }
+    }
+    // max-reductions: the max of x and the max of -x (= -min)
+    int v[8] = {in ? l0 : INT_MIN, in ? -l0 : INT_MIN, in ? -l1 : INT_MIN, in ? l1 : INT_MIN,
+                in ? u0 : INT_MIN, in ? -u0 : INT_MIN, in ? -u1 : INT_MIN, in ? u1 : INT_MIN};
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v[q] = max(v[q], __shfl_xor_sync(0xffffffffu, v[q], off));
+    __shared__ int red[4][8];
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) red[w][q] = v[q];
+    __syncthreads();
+    if (threadIdx.x < 8) {
+        int r = red[0][threadIdx.x];
+        for (int ww = 1; ww < (int)(blockDim.x >> 5); ++ww) r = max(r, red[ww][threadIdx.x]);
+        const bool neg = (threadIdx.x == 1 || threadIdx.x == 2 || threadIdx.x == 5 || threadIdx.x == 6);
+        int32_t *mm = reinterpret_cast<int32_t *>(plan + L.off_minmax) + ((int64_t)s * L.n_k + kt) * 8;
+        mm[threadIdx.x] = neg ? -r : r;
+    }
+    if (kt == 0 && s == 0 && threadIdx.x == 0) {
+        PlanHeader *h = reinterpret_cast<PlanHeader *>(plan);
+        h->B = L.B; h->Hm = L.Hm; h->N = L.N; h->bq = L.bq; h->bk = L.bk;
+        h->n_q = L.n_q; h->n_k = L.n_k; h->total = L.total;
+        __threadfence();
+        h->magic = kPlanMagic;
+    }
+}
+
+__device__ __forceinline__ TileMinMax load_minmax(const int32_t *p)
+{
+    TileMinMax t;
+    t.L0max = p[0]; t.L0min = p[1]; t.L1min = p[2]; t.L1max = p[3];
+    t.U0max = p[4]; t.U0min = p[5]; t.U1min = p[6]; t.U1max = p[7];
+    return t;
+}
+
+// blockIdx.x < n_q: row job for Q tile blockIdx.x; otherwise column job for
+// KV tile blockIdx.x - n_q.  128 threads; ordered compaction by warp ballots.
+__global__ void __launch_bounds__(128) classify_lists_kernel(PlanLayout L, uint8_t *plan,
+                                                             uint8_t *labels_out)
+{
+    const int s = blockIdx.y;
+    const int N = L.N;
+    const int32_t *mm = reinterpret_cast<const int32_t *>(plan + L.off_minmax) + (int64_t)s * L.n_k * 8;
+    __shared__ int warp_cnt[4];
+    __shared__ int base_sh;
+    const int w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    if (threadIdx.x == 0) base_sh = 0;
+    __syncthreads();
+
+    const bool row_job = (int)blockIdx.x < L.n_q;
+    const int idx = row_job ? blockIdx.x : blockIdx.x - L.n_q;
+    const int n_other = row_job ? L.n_k : L.n_q;
+    int32_t *list;
+    int32_t *cnt;
+    uint8_t *lbl_row = nullptr, *lbl_out = nullptr;
+    TileMinMax own{};
+    int qb = 0, qe = 0;
+    if (row_job) {
+        list = reinterpret_cast<int32_t *>(plan + L.off_row_list) + ((int64_t)s * L.n_q + idx) * L.n_k;
+        cnt = reinterpret_cast<int32_t *>(plan + L.off_row_cnt) + (int64_t)s * L.n_q + idx;
+        lbl_row = plan + L.off_labels + ((int64_t)s * L.n_q + idx) * L.n_k;
+        if (labels_out) lbl_out = labels_out + ((int64_t)s * L.n_q + idx) * L.n_k;
+        qb = idx * L.bq;
+        qe = min(qb + L.bq, N);
+    } else {
+        list = reinterpret_cast<int32_t *>(plan + L.off_col_list) + ((int64_t)s * L.n_k + idx) * L.n_q;
+        cnt = reinterpret_cast<int32_t *>(plan + L.off_col_cnt) + (int64_t)s * L.n_k + idx;
+        own = load_minmax(mm + (int64_t)idx * 8);
+    }
+    for (int c0 = 0; c0 < n_other; c0 += 128) {
+        const int c = c0 + threadIdx.x;
+        int lab = FM_TILE_SKIP;
+        if (c < n_other) {
+            if (row_job) {
+                lab = tile_label(load_minmax(mm + (int64_t)c * 8), qb, qe);
+                lbl_row[c] = (uint8_t)lab;
+                if (lbl_out) lbl_out[c] = (uint8_t)lab;
+            } else {
+                const int b0 = c * L.bq;
+                lab = tile_label(own, b0, min(b0 + L.bq, N));
+            }
+        }
+        const bool keep = c < n_other && lab != FM_TILE_SKIP;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (ln == 0) warp_cnt[w] = __popc(bal);
+        __syncthreads();
+        int before = base_sh;
+        for (int ww = 0; ww < w; ++ww) before += warp_cnt[ww];
+        if (keep) list[before + __popc(bal & ((1u << ln) - 1u))] = c | (lab << kLabelShift);
+        __syncthreads();
+        if (threadIdx.x == 0) base_sh += warp_cnt[0] + warp_cnt[1] + warp_cnt[2] + warp_cnt[3];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *cnt = base_sh;
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+fm_status fm_classify_launch(fm_bounds m, int bq, int bk, void *plan, uint8_t *labels,
+                             int32_t *status, cudaStream_t stream)
+{
+    PlanLayout L;
+    if (!plan_layout(m.B, m.Hm, m.N, bq, bk, &L)) return FM_ERR_INVALID_ARG;
+    const int S = m.B * m.Hm;
+    if (L.n_k > 65535 * 64 || S > 65535) return FM_ERR_UNSUPPORTED;
+    {
+        ProfScope ps(kKClassifyMinmax, stream);
+        classify_minmax_kernel<<<dim3(L.n_k, S), 128, 0, stream>>>(m, L, (uint8_t *)plan, status);
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) return FM_ERR_CUDA;
+    {
+        ProfScope ps(kKClassifyLists, stream);
+        classify_lists_kernel<<<dim3(L.n_q + L.n_k, S), 128, 0, stream>>>(L, (uint8_t *)plan, labels);
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) return FM_ERR_CUDA;
+    return FM_OK;
+}

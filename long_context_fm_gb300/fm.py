@@ -1,0 +1,260 @@
+"""Python binding of ``libfm.so`` (include/fm.h): the same entry points, with
+torch tensors and numpy arrays marshalled to pointers.  Every step of the
+computation runs inside the library; this module only checks types,
+allocates caller-owned buffers with torch where a helper says so, and
+forwards.  Importing it fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfm.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                      "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_UNREPRESENTABLE = 0, 1, 2, 3
+FM_ERR_BAD_BOUNDS, FM_ERR_PLAN_MISMATCH, FM_ERR_WORKSPACE, FM_ERR_CUDA, FM_ERR_TIMEOUT = 4, 5, 6, 7, 8
+FM_TILE_SKIP, FM_TILE_FULL, FM_TILE_PARTIAL = 0, 1, 2
+FM_DT_BF16, FM_DT_F32 = 0, 1
+KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post"]
+
+EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_plan_bytes",
+            "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
+            "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout"]
+
+
+class FmError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = int(code)
+        super().__init__(f"{where}: {fm_status_string(code)} ({code})")
+
+
+class Bounds(ctypes.Structure):
+    _fields_ = [("lts", ctypes.c_void_p), ("lte", ctypes.c_void_p), ("uts", ctypes.c_void_p),
+                ("ute", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hm", ctypes.c_int32),
+                ("N", ctypes.c_int32)]
+
+
+class KernelTime(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("ms", ctypes.c_float)]
+
+
+_P, _I, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+_lib.fm_status_string.restype = ctypes.c_char_p
+_lib.fm_status_string.argtypes = [_I]
+_lib.fm_abi_version.restype = _I
+_lib.fm_mask_from_rows.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P]
+_lib.fm_plan_bytes.restype = _SZ
+_lib.fm_plan_bytes.argtypes = [_I, _I, _I, _I, _I]
+_lib.fm_tile_classify.argtypes = [Bounds, _I, _I, _P, _SZ, _P, _P, _P]
+_lib.fm_fwd_workspace_bytes.restype = _SZ
+_lib.fm_fwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
+_lib.fm_attn_fwd.argtypes = [_P, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _P, _P]
+_lib.fm_bwd_workspace_bytes.restype = _SZ
+_lib.fm_bwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
+_lib.fm_attn_bwd.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _P, _P,
+                             _I, _P, _SZ, _P, _P]
+_lib.fm_profile_begin.argtypes = []
+_lib.fm_profile_end.restype = _I
+_lib.fm_profile_end.argtypes = [_P, _I]
+_lib.fm_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _P, _P]
+
+
+def _check(code, where):
+    if code != FM_OK:
+        raise FmError(code, where)
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return FM_DT_BF16
+    if t.dtype == torch.float32:
+        return FM_DT_F32
+    raise TypeError(f"unsupported output dtype {t.dtype}")
+
+
+def fm_status_string(code: int) -> str:
+    return _lib.fm_status_string(int(code)).decode()
+
+
+def fm_abi_version() -> int:
+    return _lib.fm_abi_version()
+
+
+def make_bounds(lts, lte, uts, ute) -> Bounds:
+    """fm_bounds from four device int32 tensors [B, Hm, N]."""
+    for n, t in zip(("lts", "lte", "uts", "ute"), (lts, lte, uts, ute)):
+        _dev(t, torch.int32, n)
+        if t.dim() != 3 or t.shape != lts.shape:
+            raise ValueError(f"{n} must be [B, Hm, N] like lts")
+    B, Hm, N = lts.shape
+    return Bounds(lts.data_ptr(), lte.data_ptr(), uts.data_ptr(), ute.data_ptr(), B, Hm, N)
+
+
+def fm_mask_from_rows(cs, ce):
+    """Host conversion of row intervals (int32 [B, Hm, N]) to column bounds."""
+    cs = np.ascontiguousarray(cs, dtype=np.int32)
+    ce = np.ascontiguousarray(ce, dtype=np.int32)
+    if cs.ndim != 3 or cs.shape != ce.shape:
+        raise ValueError("cs and ce must be int32 [B, Hm, N]")
+    B, Hm, N = cs.shape
+    out = [np.empty_like(cs) for _ in range(4)]
+    code = _lib.fm_mask_from_rows(cs.ctypes.data, ce.ctypes.data, B, Hm, N,
+                                  *[o.ctypes.data for o in out])
+    _check(code, "fm_mask_from_rows")
+    return tuple(out)
+
+
+def fm_plan_bytes(B, Hm, N, bq=128, bk=128) -> int:
+    return int(_lib.fm_plan_bytes(B, Hm, N, bq, bk))
+
+
+def fm_tile_classify(bounds: Bounds, plan, dev_status, bq=128, bk=128, labels=None, stream=None):
+    _dev(plan, torch.uint8, "plan")
+    _dev(dev_status, torch.int32, "dev_status")
+    if labels is not None:
+        _dev(labels, torch.uint8, "labels")
+    code = _lib.fm_tile_classify(bounds, bq, bk, _ptr(plan), plan.numel(), _ptr(labels),
+                                 _ptr(dev_status), _stream(stream))
+    _check(code, "fm_tile_classify")
+
+
+def fm_fwd_workspace_bytes(B, H, N, d) -> int:
+    return int(_lib.fm_fwd_workspace_bytes(B, H, N, d))
+
+
+def fm_attn_fwd(q, k, v, bounds: Bounds, plan, scale, o, lse, dev_status, ws=None, stream=None):
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, torch.bfloat16, n)
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or o.shape != q.shape:
+        raise ValueError("q, k, v, o must share the shape [B, H, N, d]")
+    _dev(o, o.dtype, "o")
+    _dev(lse, torch.float32, "lse")
+    _dev(plan, torch.uint8, "plan")
+    _dev(dev_status, torch.int32, "dev_status")
+    code = _lib.fm_attn_fwd(_ptr(q), _ptr(k), _ptr(v), bounds, _ptr(plan), B, H, N, d, float(scale),
+                            _ptr(o), _dt(o), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
+                            _ptr(dev_status), _stream(stream))
+    _check(code, "fm_attn_fwd")
+
+
+def fm_bwd_workspace_bytes(B, H, N, d) -> int:
+    return int(_lib.fm_bwd_workspace_bytes(B, H, N, d))
+
+
+def fm_attn_bwd(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk, dv, ws, dev_status,
+                stream=None):
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _dev(t, torch.bfloat16, n)
+    B, H, N, d = q.shape
+    for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _dev(t, t.dtype, n)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q")
+    if not (dq.dtype == dk.dtype == dv.dtype):
+        raise TypeError("dq, dk, dv must share one dtype")
+    _dev(lse, torch.float32, "lse")
+    _dev(ws, torch.uint8, "ws")
+    code = _lib.fm_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(lse), _ptr(dO), bounds,
+                            _ptr(plan), B, H, N, d, float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
+                            _dt(dq), _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
+    _check(code, "fm_attn_bwd")
+
+
+def fm_profile_begin():
+    _check(_lib.fm_profile_begin(), "fm_profile_begin")
+
+
+def fm_profile_end(max_entries=4096):
+    """[(kernel name, ms)] of every launch since fm_profile_begin."""
+    buf = (KernelTime * max_entries)()
+    n = _lib.fm_profile_end(buf, max_entries)
+    if n < 0:
+        raise FmError(FM_ERR_CUDA, "fm_profile_end")
+    return [(KERNEL_NAMES[buf[i].kernel], float(buf[i].ms)) for i in range(n)]
+
+
+def fm_selftest_wait_timeout(limit_cycles, dev_status, stream=None):
+    _dev(dev_status, torch.int32, "dev_status")
+    _check(_lib.fm_selftest_wait_timeout(int(limit_cycles), _ptr(dev_status), _stream(stream)),
+           "fm_selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# Convenience layer: allocates the caller-owned buffers with torch and calls
+# the entry points above.
+# ---------------------------------------------------------------------------
+class MaskedAttention:
+    """Holds the device bounds, plan and status word of one mask."""
+
+    def __init__(self, lts, lte, uts, ute, device="cuda", stream=None):
+        t = [torch.as_tensor(np.ascontiguousarray(x), dtype=torch.int32).to(device) for x in
+             (lts, lte, uts, ute)]
+        self.lts, self.lte, self.uts, self.ute = t
+        self.bounds = make_bounds(*t)
+        self.B, self.Hm, self.N = self.lts.shape
+        self.plan = torch.empty(fm_plan_bytes(self.B, self.Hm, self.N), dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.stream = stream
+        fm_tile_classify(self.bounds, self.plan, self.status, stream=stream)
+
+    def labels(self, bq=128, bk=128):
+        """Labels uint8 [B, Hm, n_q, n_k] (a separate plan of tile size bq x bk)."""
+        n_q, n_k = -(-self.N // bq), -(-self.N // bk)
+        out = torch.empty((self.B, self.Hm, n_q, n_k), dtype=torch.uint8, device=self.plan.device)
+        plan = torch.empty(fm_plan_bytes(self.B, self.Hm, self.N, bq, bk), dtype=torch.uint8,
+                           device=self.plan.device)
+        fm_tile_classify(self.bounds, plan, self.status, bq, bk, labels=out, stream=self.stream)
+        return out
+
+    def forward(self, q, k, v, scale=None, o_dtype=torch.bfloat16):
+        B, H, N, d = q.shape
+        scale = 1.0 / d ** 0.5 if scale is None else scale
+        o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        fm_attn_fwd(q, k, v, self.bounds, self.plan, scale, o, lse, self.status, stream=self.stream)
+        return o, lse
+
+    def backward(self, q, k, v, o, lse, dO, scale=None, grad_dtype=torch.float32, ws=None):
+        B, H, N, d = q.shape
+        scale = 1.0 / d ** 0.5 if scale is None else scale
+        if ws is None:
+            ws = torch.empty(fm_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+        dq, dk, dv = (torch.empty(q.shape, dtype=grad_dtype, device=q.device) for _ in range(3))
+        fm_attn_bwd(q, k, v, o, lse, dO, self.bounds, self.plan, scale, dq, dk, dv, ws, self.status,
+                    stream=self.stream)
+        return dq, dk, dv
+
+    def check_status(self):
+        code = int(self.status.item())
+        if code != 0:
+            raise FmError(code, "device")

@@ -1,0 +1,169 @@
+"""The C ABI library loads, exports every entry point of include/fm.h, and its
+host-side logic (sizes, status strings, the row-to-column converter) is right.
+No GPU is used: the converter is host code."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from long_context_fm_gb300 import build as fmbuild
+from long_context_fm_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def fm():
+    fmbuild.build()
+    from long_context_fm_gb300 import fm as mod
+    return mod
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(fm):
+    names = _declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(fm._lib, n), n
+    assert sorted(fm.EXPORTED) == names
+
+
+def test_abi_version_and_status_strings(fm):
+    assert fm.fm_abi_version() == 1
+    for code in range(9):
+        assert fm.fm_status_string(code) and "unknown" not in fm.fm_status_string(code)
+    assert "unknown" in fm.fm_status_string(99)
+
+
+def test_plan_bytes(fm):
+    assert fm.fm_plan_bytes(1, 1, 256) > 0
+    assert fm.fm_plan_bytes(1, 1, 256, 96, 128) == 0
+    assert fm.fm_plan_bytes(0, 1, 256) == 0
+    big = fm.fm_plan_bytes(1, 1, 131072)
+    n = 1024
+    assert big >= n * n * (1 + 4 + 4) and big < n * n * 10 + (1 << 20)
+    assert fm.fm_bwd_workspace_bytes(1, 8, 131072, 128) >= 8 * 131072 * 128 * 4 + 8 * 131072 * 4
+    assert fm.fm_bwd_workspace_bytes(1, 1, 10, 96) == 0
+
+
+def _cols(m, b, hm):
+    return [m[k][b, hm] for k in ("lts", "lte", "uts", "ute")]
+
+
+@pytest.mark.parametrize("name", [n for n in list(W.SMALL) + ["tiny_causal", "doc_packing",
+                                                             "sliding_window", "prefix_lm",
+                                                             "long_packing_128k"]])
+def test_converter_reproduces_generator_bounds(fm, name):
+    wl = W.SMALL.get(name) or W.FULL[name]
+    m = W.make_mask(wl)
+    if m["rows"] is None:
+        pytest.skip("no row form")
+    lts, lte, uts, ute = fm.fm_mask_from_rows(*m["rows"])
+    # the generator writes the same canonical form: bit-exact
+    assert np.array_equal(lts, m["lts"]) and np.array_equal(lte, m["lte"])
+    assert np.array_equal(uts, m["uts"]) and np.array_equal(ute, m["ute"])
+
+
+def test_converter_golden_examples(fm):
+    import json
+    gd = json.load(open(os.path.join(ROOT, "tests", "golden", "causal_row_form.json")))
+    cs = np.array(gd["col_start"], np.int32)[None, None]
+    ce = np.array(gd["col_end"], np.int32)[None, None]
+    got = fm.fm_mask_from_rows(cs, ce)
+    for arr, key in zip(got, ("lts", "lte", "uts", "ute")):
+        assert arr[0, 0].tolist() == gd["expect_columns"][key]
+    gd = json.load(open(os.path.join(ROOT, "tests", "golden", "doc_packing_example.json")))["small"]
+    got = fm.fm_mask_from_rows(np.array(gd["col_start"], np.int32)[None, None],
+                               np.array(gd["col_end"], np.int32)[None, None])
+    for arr, key in zip(got, ("lts", "lte", "uts", "ute")):
+        assert arr[0, 0].tolist() == gd["expect_columns"][key]
+
+
+def _masked_runs_per_column(M):
+    """Number of maximal masked row runs in each column of a dense mask."""
+    Mi = M.astype(np.int8)
+    starts = (Mi[0] == 1).astype(int) + ((Mi[1:] == 1) & (Mi[:-1] == 0)).sum(0)
+    return starts
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_converter_random_rows_against_dense_masks(fm, seed):
+    rng = np.random.default_rng(1000 + seed)
+    N = int(rng.integers(1, 90))
+    mode = seed % 3
+    if mode == 0:       # arbitrary intervals: often unrepresentable
+        a = rng.integers(0, N, size=N); b = rng.integers(0, N, size=N)
+        cs, ce = np.minimum(a, b), np.maximum(a, b)
+    elif mode == 1:     # monotone-ish (sliding structures): usually representable
+        cs = np.sort(rng.integers(0, N, size=N)); ce = np.maximum(cs, np.sort(rng.integers(0, N, size=N)))
+    else:               # with empty rows and full rows
+        cs = rng.integers(0, N, size=N); ce = cs + rng.integers(-3, N, size=N)
+        ce = np.minimum(ce, N - 1)
+    cs = cs.astype(np.int32); ce = ce.astype(np.int32)
+    Mr = oracle.dense_from_rows(cs, ce)
+    representable = bool((_masked_runs_per_column(Mr) <= 2).all())
+    try:
+        got = fm.fm_mask_from_rows(cs[None, None], ce[None, None])
+    except fm.FmError as e:
+        assert e.code == fm.FM_ERR_UNREPRESENTABLE and not representable
+        return
+    assert representable
+    Mc = oracle.dense_from_cols(*[g[0, 0] for g in got])
+    assert np.array_equal(Mr, Mc)
+    lts, lte, uts, ute = (g[0, 0] for g in got)
+    assert np.all((lts < lte) | ((lts == N) & (lte == N)))      # canonical empty lower
+    assert np.all((uts < ute) | ((uts == 0) & (ute == 0)))      # canonical empty upper
+
+
+def test_converter_counts_representable_cases(fm):
+    """Across many random masks both outcomes occur and always agree with brute force."""
+    rng = np.random.default_rng(77)
+    seen = {True: 0, False: 0}
+    for _ in range(200):
+        N = int(rng.integers(1, 40))
+        cs = rng.integers(0, N, size=N).astype(np.int32)
+        ce = (cs + rng.integers(-2, 12, size=N)).clip(max=N - 1).astype(np.int32)
+        Mr = oracle.dense_from_rows(cs, ce)
+        rep = bool((_masked_runs_per_column(Mr) <= 2).all())
+        try:
+            got = fm.fm_mask_from_rows(cs[None, None], ce[None, None])
+            assert rep
+            assert np.array_equal(Mr, oracle.dense_from_cols(*[g[0, 0] for g in got]))
+        except fm.FmError as e:
+            assert e.code == fm.FM_ERR_UNREPRESENTABLE and not rep
+        seen[rep] += 1
+    assert seen[True] > 20 and seen[False] > 20
+
+
+def test_converter_rejects_bad_rows(fm):
+    cs = np.array([[[0, 0, 5]]], np.int32)
+    ce = np.array([[[0, 1, 7]]], np.int32)            # ce = 7 >= N = 3
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_mask_from_rows(cs, ce)
+    assert e.value.code == fm.FM_ERR_BAD_BOUNDS
+    cs = np.array([[[-1, 0, 0]]], np.int32)
+    ce = np.array([[[0, 1, 2]]], np.int32)
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_mask_from_rows(cs, ce)
+    assert e.value.code == fm.FM_ERR_BAD_BOUNDS
+    # empty rows (cs > ce) are fine anywhere
+    out = fm.fm_mask_from_rows(np.array([[[2, 0, 0]]], np.int32), np.array([[[1, 0, 2]]], np.int32))
+    assert out[0].shape == (1, 1, 3)
+
+
+def test_converter_batches_and_heads(fm):
+    wl = W.SMALL["docs_small"].with_(Hm=1)
+    m = W.make_mask(wl)
+    cs, ce = m["rows"]
+    cs2 = np.concatenate([cs, cs[:, :, ::-1] * 0], axis=1)      # second head: causal (cs = 0)
+    ce2 = np.concatenate([ce, np.broadcast_to(np.arange(wl.N, dtype=np.int32), ce.shape)], axis=1)
+    got = fm.fm_mask_from_rows(cs2, ce2)
+    assert np.array_equal(got[0][:, :1], m["lts"]) and np.array_equal(got[3][:, :1], m["ute"])
+    assert np.all(got[3][:, 1] == np.arange(wl.N)) and np.all(got[0][:, 1] == wl.N)

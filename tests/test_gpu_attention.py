@@ -1,0 +1,194 @@
+"""Forward and backward on the GPU against the oracle, element by element, on
+sizes that span several tiles and a ragged tail; invariants; failure paths."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from long_context_fm_gb300 import workloads as W
+from parity import check_close, check_lse, run_fm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fm():
+    from long_context_fm_gb300 import fm as mod
+    return mod
+
+
+@pytest.mark.parametrize("name", list(W.SMALL))
+def test_fwd_bwd_match_oracle(fm, name):
+    wl = W.SMALL[name]
+    m = W.make_mask(wl)
+    q, k, v, dO = W.make_inputs(wl)
+    out = run_fm(fm, wl, m, q, k, v, dO)
+    O, L = oracle.forward(q, k, v, m, wl.scale)
+    g = oracle.backward(q, k, v, dO, m, wl.scale)
+    check_close("O", out["o"].cpu().numpy(), O)
+    check_lse(out["lse"].cpu().numpy(), L)
+    check_close("dQ", out["dq"].cpu().numpy(), g["dq"])
+    check_close("dK", out["dk"].cpu().numpy(), g["dk"])
+    check_close("dV", out["dv"].cpu().numpy(), g["dv"])
+
+
+@pytest.mark.parametrize("name", ["docs_small", "random_cols_d64", "causal_ragged"])
+def test_bf16_outputs(fm, name):
+    """bf16 outputs: the same values up to one bf16 rounding of each output."""
+    wl = W.SMALL[name]
+    m = W.make_mask(wl)
+    q, k, v, dO = W.make_inputs(wl)
+    out = run_fm(fm, wl, m, q, k, v, dO, o_dtype=torch.bfloat16, g_dtype=torch.bfloat16)
+    O, L = oracle.forward(q, k, v, m, wl.scale)
+    g = oracle.backward(q, k, v, dO, m, wl.scale)
+    check_close("O", out["o"].float().cpu().numpy(), O)
+    check_lse(out["lse"].cpu().numpy(), L)
+    for key in ("dq", "dk", "dv"):
+        check_close(key, out[key].float().cpu().numpy(), g[key])
+
+
+def test_full_ragged_multi_tile_causal_d128(fm):
+    wl = W.Workload("causal_1000", B=2, H=3, N=1000, d=128, mask="causal")
+    m = W.make_mask(wl)
+    q, k, v, dO = W.make_inputs(wl, seed=4)
+    out = run_fm(fm, wl, m, q, k, v, dO)
+    O, L = oracle.forward(q, k, v, m, wl.scale)
+    g = oracle.backward(q, k, v, dO, m, wl.scale)
+    check_close("O", out["o"].cpu().numpy(), O)
+    check_lse(out["lse"].cpu().numpy(), L)
+    for key in ("dq", "dk", "dv"):
+        check_close(key, out[key].cpu().numpy(), g[key])
+
+
+def test_single_row_and_tiny_n(fm):
+    for N in (1, 7, 64, 129):
+        wl = W.Workload(f"c{N}", B=1, H=1, N=N, d=64, mask="causal")
+        m = W.make_mask(wl)
+        q, k, v, dO = W.make_inputs(wl, seed=N)
+        out = run_fm(fm, wl, m, q, k, v, dO)
+        O, L = oracle.forward(q, k, v, m, wl.scale)
+        g = oracle.backward(q, k, v, dO, m, wl.scale)
+        check_close("O", out["o"].cpu().numpy(), O)
+        check_lse(out["lse"].cpu().numpy(), L)
+        for key in ("dq", "dk", "dv"):
+            check_close(key, out[key].cpu().numpy(), g[key])
+
+
+def test_constant_v_and_dead_rows(fm):
+    """Constant V returns V on every row that attends something; rows that
+    attend nothing return O = 0 and lse = -inf; columns nobody attends get
+    dK = dV = 0."""
+    N, d = 300, 128
+    lts = np.full(N, N, np.int32); lte = np.full(N, N, np.int32)
+    uts = np.zeros(N, np.int32); ute = np.maximum(np.arange(N), 150).astype(np.int32)
+    ute[20:40] = 0; lts[20:40] = 100; lte[20:40] = 150      # rows < 100 see columns 20..39 only
+    ute[-5:] = N                                            # last five columns: nobody
+    m = {k: x[None, None] for k, x in zip(("lts", "lte", "uts", "ute"), (lts, lte, uts, ute))}
+    wl = W.Workload("inv", B=1, H=2, N=N, d=d, mask="causal")
+    g = torch.Generator().manual_seed(9)
+    q, k, dO = (torch.randn(1, 2, N, d, generator=g).to(torch.bfloat16) for _ in range(3))
+    vrow = torch.randn(d, generator=g).to(torch.bfloat16)
+    v = vrow.expand(1, 2, N, d).contiguous()
+    out = run_fm(fm, wl, m, q, k, v, dO)
+    M = oracle.dense_from_cols(lts, lte, uts, ute)
+    live = ~M.all(1)
+    o = out["o"].cpu().numpy()[0]
+    assert (~live).sum() == 50                               # rows 100..149 see nothing
+    np.testing.assert_allclose(o[:, live], np.broadcast_to(vrow.float().numpy(), (2, live.sum(), d)),
+                               atol=1e-5)
+    assert np.all(o[:, ~live] == 0)
+    assert np.all(out["lse"].cpu().numpy()[0, :, ~live] == -np.inf)
+    assert np.all(out["dq"].cpu().numpy()[0, :, ~live] == 0)
+    never = M.all(0)
+    assert np.all(out["dk"].cpu().numpy()[0, :, never] == 0) and np.all(out["dv"].cpu().numpy()[0, :, never] == 0)
+
+
+def test_single_attended_key(fm):
+    """A row that attends one key returns that key's value row, lse = its score."""
+    N, d = 256, 64
+    lts = np.full(N, N, np.int32); lte = np.full(N, N, np.int32)
+    uts = np.zeros(N, np.int32); ute = np.full(N, N, np.int32)   # everything masked ...
+    ute[17] = 0; lts[17] = 200                                   # ... but column 17 for rows < 200
+    m = {k: x[None, None] for k, x in zip(("lts", "lte", "uts", "ute"), (lts, lte, uts, ute))}
+    wl = W.Workload("one", B=1, H=1, N=N, d=d, mask="causal")
+    q, k, v, dO = W.make_inputs(wl.with_(N=N), seed=3)
+    out = run_fm(fm, wl, m, q, k, v, dO)
+    o = out["o"].cpu().numpy()[0, 0]
+    np.testing.assert_allclose(o[:200], np.broadcast_to(v[0, 0, 17].float().numpy(), (200, d)), atol=1e-6)
+    s = wl.scale * (q[0, 0, :200].double() @ k[0, 0, 17].double()).numpy()
+    np.testing.assert_allclose(out["lse"].cpu().numpy()[0, 0, :200], s, atol=1e-3)
+
+
+def test_deterministic_forward(fm):
+    wl = W.SMALL["prefix_random_small"]
+    m = W.make_mask(wl)
+    q, k, v, dO = W.make_inputs(wl)
+    a = run_fm(fm, wl, m, q, k, v)
+    b = run_fm(fm, wl, m, q, k, v)
+    assert torch.equal(a["o"], b["o"]) and torch.equal(a["lse"], b["lse"])
+
+
+def test_plan_mismatch_reported(fm):
+    wl = W.SMALL["docs_small"]
+    m = W.make_mask(wl)
+    q, k, v, _ = W.make_inputs(wl)
+    att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"])
+    plan64 = torch.empty(fm.fm_plan_bytes(wl.B, 1, wl.N, 64, 64), dtype=torch.uint8, device="cuda")
+    fm.fm_tile_classify(att.bounds, plan64, att.status, 64, 64)
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    big = torch.empty(max(plan64.numel(), att.plan.numel()), dtype=torch.uint8, device="cuda")
+    big[: plan64.numel()].copy_(plan64)
+    fm.fm_attn_fwd(q.cuda(), k.cuda(), v.cuda(), att.bounds, big, wl.scale, o, lse, att.status)
+    torch.cuda.synchronize()
+    assert int(att.status.item()) == fm.FM_ERR_PLAN_MISMATCH
+
+
+def test_host_rejects_bad_arguments(fm):
+    wl = W.SMALL["causal_ragged"]
+    m = W.make_mask(wl)
+    q, k, v, _ = W.make_inputs(wl)
+    att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"])
+    qd = q.cuda()
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_attn_fwd(qd, qd, qd, att.bounds, att.plan, -1.0, o, lse, att.status)
+    assert e.value.code == fm.FM_ERR_INVALID_ARG
+    q96 = torch.zeros((1, 1, 64, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fm.FmError) as e:
+        fm.fm_attn_fwd(q96, q96, q96, att.bounds, att.plan, 0.1, torch.empty_like(q96, dtype=torch.float32),
+                       torch.empty((1, 1, 64), device="cuda"), att.status)
+    assert e.value.code in (fm.FM_ERR_UNSUPPORTED, fm.FM_ERR_INVALID_ARG)
+    with pytest.raises(fm.FmError) as e:
+        ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+        g = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        fm.fm_attn_bwd(qd, qd, qd, o, lse, qd, att.bounds, att.plan, 0.1, g, g, g, ws, att.status)
+    assert e.value.code == fm.FM_ERR_WORKSPACE
+
+
+def test_bounded_wait_times_out_and_context_survives(fm):
+    """A wait that nothing completes returns FM_ERR_TIMEOUT instead of hanging,
+    and the GPU context keeps working afterwards."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fm.fm_selftest_wait_timeout(20_000_000, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == fm.FM_ERR_TIMEOUT
+    wl = W.FULL["tiny_causal"]
+    m = W.make_mask(wl)
+    q, k, v, _ = W.make_inputs(wl)
+    out = run_fm(fm, wl, m, q, k, v)
+    O, _ = oracle.forward(q, k, v, m, wl.scale)
+    check_close("O", out["o"].cpu().numpy(), O)
+
+
+def test_profiler_records_every_launch(fm):
+    wl = W.SMALL["docs_small"]
+    m = W.make_mask(wl)
+    q, k, v, dO = W.make_inputs(wl)
+    fm.fm_profile_begin()
+    run_fm(fm, wl, m, q, k, v, dO)
+    rec = fm.fm_profile_end()
+    names = [r[0] for r in rec]
+    assert names == ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post"]
+    assert all(ms > 0 for _, ms in rec)
