@@ -75,7 +75,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -133,6 +133,16 @@ def total_pairs(wl, m):
     return tot
 
 
+def max_over_ranks(vals, world, device):
+    """Element-wise max of per-rank timings (the only collective of the run)."""
+    t = torch.tensor(vals, dtype=torch.float64)
+    if world > 1:
+        t = t.to(device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t = t.cpu()
+    return [float(x) for x in t]
+
+
 def run_fm(args, rank, world, local_rank):
     from long_context_fm_gb300 import fm
 
@@ -178,7 +188,9 @@ def run_fm(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     fm.fm_profile_begin()
-    with ClockSampler(local_rank) as clocks:
+    uuid = str(getattr(torch.cuda.get_device_properties(dev), "uuid", "") or "")
+    smi_id = (uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") if uuid else str(local_rank)
+    with ClockSampler(smi_id) as clocks:
         ev0.record(stream)
         for _ in range(args.steps):
             step()
@@ -228,13 +240,7 @@ def run_fm(args, rank, world, local_rank):
     barrier()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
-    # max over ranks
-    t = torch.tensor([ms_step, e2e_s], dtype=torch.float64)
-    if world > 1:
-        t = t.to(dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t = t.cpu()
-    ms_step, e2e_s = float(t[0]), float(t[1])
+    ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
                 avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h)
 
@@ -264,8 +270,8 @@ def cpu_baseline_sample(wl, m, max_docs=3):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="fm", choices=["fm", "reference"])
     ap.add_argument("--config", default="long_packing_128k", choices=list(W.FULL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -333,7 +339,7 @@ def main():
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
         }
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline_sample(wl, W.make_mask(wl), max_docs=1)
+            line["cpu_baseline"] = cpu_baseline_sample(wl, W.make_mask(wl), max_docs=7)
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

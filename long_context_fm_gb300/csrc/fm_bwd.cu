@@ -20,7 +20,9 @@
 //   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
 //   dP^T = V dO^T       (SS, K-major/K-major)        -> TMEM
 //   P^T  = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T o (dP^T - D)
-//          written as bf16 into 128-byte-swizzled shared memory
+//          each written as two bf16 terms (hi + lo, ~16 significant bits)
+//          into 128-byte-swizzled shared memory; the MMAs below consume both
+//          terms, so the gradients do not carry a bf16 rounding of P or dS
 //   dV  += P^T dO       (SS, P^T K-major, dO MN-major)
 //   dK  += dS^T Q       (SS, dS^T K-major, Q MN-major)
 //   dQ^T = K^T dS^T     (SS, K MN-major, dS^T MN-major)
@@ -99,12 +101,15 @@ struct BwdSmem {
     static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
     static constexpr int kKTile = 128 * D * 2;
     static constexpr int kQTile = 64 * D * 2;
+    static constexpr int kOp = 128 * 128;       // one 128 x 64 bf16 operand tile
     static constexpr int kK = 0, kV = kKTile;
     static constexpr int kQ = 2 * kKTile;                 // [2] stages
     static constexpr int kdO = kQ + 2 * kQTile;           // [2] stages
-    static constexpr int kP = kdO + 2 * kQTile;           // 128 x 64 bf16
-    static constexpr int kdS = kP + 128 * 128;
-    static constexpr int kStat = kdS + 128 * 128;         // lse2 [2][64], D [2][64]
+    static constexpr int kP = kdO + 2 * kQTile;           // P^T  high part
+    static constexpr int kPlo = kP + kOp;                 // P^T  low part
+    static constexpr int kdS = kPlo + kOp;                // dS^T high part
+    static constexpr int kdSlo = kdS + kOp;               // dS^T low part
+    static constexpr int kStat = kdSlo + kOp;             // lse2 [2][64], D [2][64]
     static constexpr int kBar = kStat + 4 * 64 * 4;
     static constexpr int kNumBar = 16;
     static constexpr int kMisc = kBar + kNumBar * 8;
@@ -116,6 +121,15 @@ enum {
     BB_KV = 0, BB_QF0, BB_QF1, BB_QE0, BB_QE1, BB_SF, BB_SE, BB_PF, BB_DSE, BB_DQF, BB_DQE, BB_ACC,
     BB_DRAIN
 };
+
+// x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
+// 16 significant bits, so products summed by the tensor core from both
+// halves lose far less than one bf16 rounding of x.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo)
+{
+    hi = pack_bf16x2(x0, x1);
+    lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
+}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
@@ -130,7 +144,7 @@ __global__ void __launch_bounds__(320, 1)
                                                 ~uintptr_t(1023));
     uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
     uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
-    uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS;
+    uint8_t *sP = smem + S::kP, *sPlo = smem + S::kPlo, *sdS = smem + S::kdS, *sdSlo = smem + S::kdSlo;
     float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [2][64]
     float *sD = sLse + 128;                                          // [2][64]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
@@ -182,120 +196,131 @@ __global__ void __launch_bounds__(320, 1)
     const int cnt = *cnt_sh;
     const int32_t *list =
         reinterpret_cast<const int32_t *>(a.plan + L.off_col_list) + ((int64_t)sidx * L.n_k + kt) * L.n_q;
+    // Flat iteration over 64-row halves of the listed Q tiles.  Only the last
+    // Q tile can have a second half beyond N, and it is last in the list.
+    const int n_it = (cnt > 0 && (list[cnt - 1] & kTileMask) * 128 + 64 >= N) ? 2 * cnt - 1 : 2 * cnt;
+    auto q0_of = [&](int it) { return (list[it >> 1] & kTileMask) * 128 + (it & 1) * 64; };
 
     if (*ok_sh) {
         if (warp == 0) {
             // ------------------------------------------------ producer
-            if (lane == 0) {
+            if (lane == 0 && n_it > 0) {
                 tma_prefetch_desc(&tq); tma_prefetch_desc(&tk);
                 tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
-                if (cnt > 0) {
-                    mbar_arrive_expect_tx(&bars[BB_KV], 2 * S::kKTile);
+                mbar_arrive_expect_tx(&bars[BB_KV], 2 * S::kKTile);
 #pragma unroll
-                    for (int x = 0; x < NBOX; ++x) {
-                        tma_load_3d(sK + x * S::kKBox, &tk, &bars[BB_KV], x * 64, kb, bh);
-                        tma_load_3d(sV + x * S::kKBox, &tv, &bars[BB_KV], x * 64, kb, bh);
-                    }
+                for (int x = 0; x < NBOX; ++x) {
+                    tma_load_3d(sK + x * S::kKBox, &tk, &bars[BB_KV], x * 64, kb, bh);
+                    tma_load_3d(sV + x * S::kKBox, &tv, &bars[BB_KV], x * 64, kb, bh);
                 }
             }
             int it = 0;
-            bool ok = true;
-            for (int t = 0; t < cnt && ok; ++t) {
-                const int qtile = list[t] & kTileMask;
-                for (int half = 0; half < 2; ++half) {
-                    const int q0 = qtile * 128 + half * 64;
-                    if (q0 >= N) continue;
-                    const int st = it & 1;
-                    if (it >= 2 && !warp_wait(&bars[BB_QE0 + st], ((it >> 1) - 1) & 1, abort, a.status)) {
-                        ok = false;
-                        break;
-                    }
+            for (; it < n_it; ++it) {
+                const int q0 = q0_of(it);
+                const int st = it & 1;
+                if (it >= 2 && !warp_wait(&bars[BB_QE0 + st], ((it >> 1) - 1) & 1, abort, a.status)) break;
 #pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int r = lane + rr * 32, qi = q0 + r;
-                        float l2 = INFINITY, dd = 0.f;
-                        if (qi < N) {
-                            const float lv = a.lse[(int64_t)bh * N + qi];
-                            l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
-                            dd = a.Dvec[(int64_t)bh * N + qi];
-                        }
-                        sLse[st * 64 + r] = l2;
-                        sD[st * 64 + r] = dd;
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = lane + rr * 32, qi = q0 + r;
+                    float l2 = INFINITY, dd = 0.f;     // rows beyond N: P = 0
+                    if (qi < N) {
+                        const float lv = a.lse[(int64_t)bh * N + qi];
+                        l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
+                        dd = a.Dvec[(int64_t)bh * N + qi];
                     }
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
+                    sLse[st * 64 + r] = l2;
+                    sD[st * 64 + r] = dd;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
 #pragma unroll
-                        for (int x = 0; x < NBOX; ++x) {
-                            tma_load_3d(sQ + st * S::kQTile + x * S::kQBox, &tq, &bars[BB_QF0 + st], x * 64, q0, bh);
-                            tma_load_3d(sdO + st * S::kQTile + x * S::kQBox, &tdo, &bars[BB_QF0 + st], x * 64, q0, bh);
-                        }
-                    } else {
-                        mbar_arrive(&bars[BB_QF0 + st]);
+                    for (int x = 0; x < NBOX; ++x) {
+                        tma_load_3d(sQ + st * S::kQTile + x * S::kQBox, &tq, &bars[BB_QF0 + st], x * 64, q0, bh);
+                        tma_load_3d(sdO + st * S::kQTile + x * S::kQBox, &tdo, &bars[BB_QF0 + st], x * 64, q0, bh);
                     }
-                    ++it;
+                } else {
+                    mbar_arrive(&bars[BB_QF0 + st]);
                 }
             }
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
-                if (cnt > 0) mbar_wait_drain(&bars[BB_KV], 0, a.status);
+                if (n_it > 0) mbar_wait_drain(&bars[BB_KV], 0, a.status);
                 for (int k2 = (it > 2 ? it - 2 : 0); k2 < it; ++k2)
                     mbar_wait_drain(&bars[BB_QF0 + (k2 & 1)], (k2 >> 1) & 1, a.status);
             }
         } else if (warp == 1) {
             // ------------------------------------------------ MMA issuer
-            if (lane == 0) {
+            // Issue order per half `it`: S/dP of it+1 as soon as the S buffer
+            // is drained, then dV, dK, dQ of it; the tensor core computes the
+            // next scores while the P/dS warps work on the current ones.
+            if (lane == 0 && n_it > 0) {
                 constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
                 constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
                 constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
-                const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aP = smem_u32(sP), adS = smem_u32(sdS);
-                bool ok = cnt > 0 && mbar_wait(&bars[BB_KV], 0, abort, a.status);
+                const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+                const uint32_t aP[2] = {smem_u32(sP), smem_u32(sPlo)};
+                const uint32_t adS[2] = {smem_u32(sdS), smem_u32(sdSlo)};
+                auto issue_scores = [&](int it) {
+                    const int st = it & 1;
+                    const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                        const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                        mma_ss(tS, sdesc_sw128(aK + ok_, 16, 1024), sdesc_sw128(aQ + oq, 16, 1024), idS, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                        const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                        mma_ss(tdP, sdesc_sw128(aV + ok_, 16, 1024), sdesc_sw128(adO + oq, 16, 1024), idS, kk > 0);
+                    }
+                    tc_commit(&bars[BB_SF]);
+                };
+                bool ok = mbar_wait(&bars[BB_KV], 0, abort, a.status) && mbar_wait(&bars[BB_QF0], 0, abort, a.status);
+                if (ok) {
+                    tc_fence_after();
+                    issue_scores(0);
+                }
                 int it = 0;
-                for (int t = 0; t < cnt && ok; ++t) {
-                    const int qtile = list[t] & kTileMask;
-                    for (int half = 0; half < 2 && ok; ++half) {
-                        const int q0 = qtile * 128 + half * 64;
-                        if (q0 >= N) continue;
-                        const int st = it & 1;
-                        const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
-                        if (!mbar_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
-                        if (it > 0 && !mbar_wait(&bars[BB_SE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                for (; ok && it < n_it; ++it) {
+                    const int st = it & 1;
+                    if (it + 1 < n_it) {
+                        if (!mbar_wait(&bars[BB_QF0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, abort, a.status) ||
+                            !mbar_wait(&bars[BB_SE], it & 1, abort, a.status)) { ok = false; break; }
                         tc_fence_after();
+                        issue_scores(it + 1);
+                    }
+                    if (!mbar_wait(&bars[BB_PF], it & 1, abort, a.status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
-                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tS, sdesc_sw128(aK + ok_, 16, 1024), sdesc_sw128(aQ + oq, 16, 1024), idS, kk > 0);
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
-                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tdP, sdesc_sw128(aV + ok_, 16, 1024), sdesc_sw128(adO + oq, 16, 1024), idS, kk > 0);
-                        }
-                        tc_commit(&bars[BB_SF]);
-                        if (!mbar_wait(&bars[BB_PF], it & 1, abort, a.status)) { ok = false; break; }
-                        tc_fence_after();
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tdV, sdesc_sw128(aP + kk * 32, 16, 1024),
-                                   sdesc_sw128(adO + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || kk > 0));
+                            mma_ss(tdV, sdesc_sw128(aP[part] + kk * 32, 16, 1024),
+                                   sdesc_sw128(adO + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || part > 0 || kk > 0));
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tdK, sdesc_sw128(adS + kk * 32, 16, 1024),
-                                   sdesc_sw128(aQ + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || kk > 0));
-                        if (it > 0 && !mbar_wait(&bars[BB_DQE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
-                        tc_fence_after();
+                            mma_ss(tdK, sdesc_sw128(adS[part] + kk * 32, 16, 1024),
+                                   sdesc_sw128(aQ + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || part > 0 || kk > 0));
+                    if (it > 0 && !mbar_wait(&bars[BB_DQE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_ss(tdQ, sdesc_sw128(aK + kk * 2048, S::kKBox, 1024),
-                                   sdesc_sw128(adS + kk * 2048, S::kKBox, 1024), idQ, kk > 0);
-                        tc_commit(&bars[BB_DQF]);
-                        tc_commit(&bars[BB_DSE]);
-                        tc_commit(&bars[BB_QE0 + st]);
-                        ++it;
-                    }
+                                   sdesc_sw128(adS[part] + kk * 2048, S::kKBox, 1024), idQ, (part > 0 || kk > 0));
+                    tc_commit(&bars[BB_DQF]);
+                    tc_commit(&bars[BB_DSE]);
+                    tc_commit(&bars[BB_QE0 + st]);
                 }
-                if (ok && it > 0) tc_commit(&bars[BB_ACC]);
+                if (ok) tc_commit(&bars[BB_ACC]);
+            }
+            if (lane == 0) {
                 tc_commit(&bars[BB_DRAIN]);
                 mbar_wait_drain(&bars[BB_DRAIN], 0, a.status);
             }
@@ -312,79 +337,71 @@ __global__ void __launch_bounds__(320, 1)
                 lo0 = l0; lolen = max(l1 - l0, 0); up0 = u0; uplen = max(u1 - u0, 0);
             }
             const bool kv_tail = kb + 128 > N;
-            int it = 0;
             bool ok = true;
-            for (int t = 0; t < cnt && ok; ++t) {
-                const int32_t e = list[t];
-                const int qtile = e & kTileMask, lab = e >> kLabelShift;
-                const bool pred = (lab == FM_TILE_PARTIAL) || kv_tail;
-                for (int half = 0; half < 2; ++half) {
-                    const int q0 = qtile * 128 + half * 64;
-                    if (q0 >= N) continue;
-                    const int st = it & 1;
-                    if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
-                        !warp_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const float *l2 = sLse + st * 64;
-                    const float *dd = sD + st * 64;
-                    // P^T row: exp2(s * scale*log2e - lse*log2e), masked -> 0.
-                    float p[64];
-                    {
-                        uint32_t raw[2][32];
-                        tmem_ld32(tS + lane_off, raw[0]);
-                        tmem_ld32(tS + lane_off + 32, raw[1]);
-                        tmem_ld_wait();
-                        tmem_reg_fence(raw[0]);
-                        tmem_reg_fence(raw[1]);
-#pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            float pv = ex2(fmaf(__uint_as_float(raw[c >> 5][c & 31]), a.scale_log2, -l2[c]));
-                            if (pred) {
-                                const int qi = q0 + c;
-                                const bool msk = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
-                                                 ((unsigned)(qi - up0) < (unsigned)uplen);
-                                pv = msk ? 0.f : pv;
-                            }
-                            p[c] = pv;
-                        }
-                    }
-                    uint32_t draw[2][32];
-                    tmem_ld32(tdP + lane_off, draw[0]);
-                    tmem_ld32(tdP + lane_off + 32, draw[1]);
+            int it = 0;
+            for (; it < n_it; ++it) {
+                const int q0 = q0_of(it);
+                const bool pred = ((list[it >> 1] >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
+                const int st = it & 1;
+                if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
+                    !warp_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                tc_fence_after();
+                const float *l2 = sLse + st * 64;
+                const float *dd = sD + st * 64;
+                // P^T row: exp2(s * scale*log2e - lse*log2e), masked -> 0.
+                float p[64];
+                {
+                    uint32_t raw[2][32];
+                    tmem_ld32(tS + lane_off, raw[0]);
+                    tmem_ld32(tS + lane_off + 32, raw[1]);
                     tmem_ld_wait();
-                    tmem_reg_fence(draw[0]);
-                    tmem_reg_fence(draw[1]);
-                    tc_fence_before();
-                    mbar_arrive(&bars[BB_SE]);      // S^T and dP^T may now be overwritten
-                    if (it > 0 && !warp_wait(&bars[BB_DSE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
-                    // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
-                    uint8_t *prow = sP + r * 128;
-                    uint8_t *drow = sdS + r * 128;
+                    tmem_reg_fence(raw[0]);
+                    tmem_reg_fence(raw[1]);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint32_t pw[4], dw[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int c0 = 8 * c + 2 * u;
-                            const float ds0 = p[c0] * (__uint_as_float(draw[c0 >> 5][c0 & 31]) - dd[c0]);
-                            const float ds1 = p[c0 + 1] * (__uint_as_float(draw[(c0 + 1) >> 5][(c0 + 1) & 31]) - dd[c0 + 1]);
-                            pw[u] = pack_bf16x2(p[c0], p[c0 + 1]);
-                            dw[u] = pack_bf16x2(ds0, ds1);
+                    for (int c = 0; c < 64; ++c) {
+                        float pv = ex2(fmaf(__uint_as_float(raw[c >> 5][c & 31]), a.scale_log2, -l2[c]));
+                        if (pred) {
+                            const int qi = q0 + c;
+                            const bool msk = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
+                                             ((unsigned)(qi - up0) < (unsigned)uplen);
+                            pv = msk ? 0.f : pv;
                         }
-                        const int pc = (c ^ (r & 7)) << 4;
-                        *reinterpret_cast<uint4 *>(prow + pc) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                        *reinterpret_cast<uint4 *>(drow + pc) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+                        p[c] = pv;
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bars[BB_PF]);
-                    ++it;
                 }
+                uint32_t draw[2][32];
+                tmem_ld32(tdP + lane_off, draw[0]);
+                tmem_ld32(tdP + lane_off + 32, draw[1]);
+                tmem_ld_wait();
+                tmem_reg_fence(draw[0]);
+                tmem_reg_fence(draw[1]);
+                tc_fence_before();
+                mbar_arrive(&bars[BB_SE]);      // S^T and dP^T may now be overwritten
+                if (it > 0 && !warp_wait(&bars[BB_DSE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
+                const int rowoff = r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t ph[4], pl[4], dh[4], dl[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c0 = 8 * c + 2 * u;
+                        const float ds0 = p[c0] * (__uint_as_float(draw[c0 >> 5][c0 & 31]) - dd[c0]);
+                        const float ds1 = p[c0 + 1] * (__uint_as_float(draw[(c0 + 1) >> 5][(c0 + 1) & 31]) - dd[c0 + 1]);
+                        split_bf16x2(p[c0], p[c0 + 1], ph[u], pl[u]);
+                        split_bf16x2(ds0, ds1, dh[u], dl[u]);
+                    }
+                    const int off = rowoff + ((c ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(sP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                    *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                    *reinterpret_cast<uint4 *>(sdS + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
+                    *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[BB_PF]);
             }
             // ------------------------------------------------ dK, dV epilogue
-            if (ok && (it == 0 || warp_wait(&bars[BB_ACC], 0, abort, a.status))) {
+            if (ok && (n_it == 0 || warp_wait(&bars[BB_ACC], 0, abort, a.status))) {
                 tc_fence_after();
                 const bool row_in = j < N;
                 const int64_t row = (int64_t)bh * N + j;
@@ -396,7 +413,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t v[32];
-                        if (it > 0) {            // warp-uniform: every lane loads
+                        if (n_it > 0) {            // warp-uniform: every lane loads
                             tmem_ld32(tsrc + lane_off + c * 32, v);
                             tmem_ld_wait();
                             tmem_reg_fence(v);
@@ -406,19 +423,19 @@ __global__ void __launch_bounds__(320, 1)
                         }
                         if (!row_in) continue;
                         if (a.g_f32) {
-                            float4 *p = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + c * 32);
+                            float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + c * 32);
 #pragma unroll
                             for (int u = 0; u < 8; ++u)
-                                p[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
-                                                   __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
+                                pp[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
+                                                    __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
                         } else {
-                            uint4 *p = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + c * 32);
+                            uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + c * 32);
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
-                                p[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
-                                                  pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
-                                                  pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
-                                                  pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
+                                pp[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
+                                                   pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
+                                                   pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
+                                                   pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
                         }
                     }
                 }
@@ -428,30 +445,23 @@ __global__ void __launch_bounds__(320, 1)
             const int quarter = warp & 3;
             const int dd = quarter * 32 + lane;      // head-dim index = TMEM lane of dQ^T
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-            int it = 0;
-            bool ok = true;
-            for (int t = 0; t < cnt && ok; ++t) {
-                const int qtile = list[t] & kTileMask;
-                for (int half = 0; half < 2; ++half) {
-                    const int q0 = qtile * 128 + half * 64;
-                    if (q0 >= N) continue;
-                    if (!warp_wait(&bars[BB_DQF], it & 1, abort, a.status)) { ok = false; break; }
-                    tc_fence_after();
-                    uint32_t v[2][32];
-                    tmem_ld32(tdQ + lane_off, v[0]);
-                    tmem_ld32(tdQ + lane_off + 32, v[1]);
-                    tmem_ld_wait();
-                    tmem_reg_fence(v[0]); tmem_reg_fence(v[1]);
-                    tc_fence_before();
-                    mbar_arrive(&bars[BB_DQE]);
-                    if (dd < D) {
-                        float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
-                        const int lim = min(64, N - q0);
+            for (int it = 0; it < n_it; ++it) {
+                const int q0 = q0_of(it);
+                if (!warp_wait(&bars[BB_DQF], it & 1, abort, a.status)) break;
+                tc_fence_after();
+                uint32_t v[2][32];
+                tmem_ld32(tdQ + lane_off, v[0]);
+                tmem_ld32(tdQ + lane_off + 32, v[1]);
+                tmem_ld_wait();
+                tmem_reg_fence(v[0]); tmem_reg_fence(v[1]);
+                tc_fence_before();
+                mbar_arrive(&bars[BB_DQE]);
+                if (dd < D) {
+                    float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
+                    const int lim = min(64, N - q0);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
-                    }
-                    ++it;
+                    for (int c = 0; c < 64; ++c)
+                        if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
                 }
             }
         }

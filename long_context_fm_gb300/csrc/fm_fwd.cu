@@ -13,8 +13,8 @@
 //   warp 1      allocates TMEM, one thread issues the tcgen05 MMAs;
 //   warps 2-5   softmax, one thread per Q row = TMEM lane.
 // TMEM (256 columns): S = Q K^T at columns [0, 128) (fp32), then overwritten
-// in place by P as packed bf16 (64 columns) which is the A operand of
-// O += P V; O accumulates at columns [128, 128 + d).
+// in place by P as two packed-bf16 terms (P_hi, P_lo: 64 columns each), the A
+// operands of O += P_hi V + P_lo V; O accumulates at columns [128, 128 + d).
 // Online softmax in the base-2 domain with a lazy rescale: O and l are
 // rescaled only when the row max grows by more than 2^8, which keeps every
 // P <= 256 and leaves the final O / l unchanged.
@@ -166,9 +166,11 @@ __global__ void __launch_bounds__(192, 2)
                         if (!mbar_wait(&bars[FB_V], t & 1, abort, a.status)) break;
                         tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tO, tS + kk * 8, sdesc_sw128(aV + kk * 2048, S::kBox, 1024), idO,
-                                   (t > 0 || kk > 0));
+                        for (int part = 0; part < 2; ++part)     // P_hi V, then P_lo V
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_ts(tO, tS + part * 64 + kk * 8, sdesc_sw128(aV + kk * 2048, S::kBox, 1024),
+                                       idO, (t > 0 || part > 0 || kk > 0));
                         tc_commit(&bars[FB_O]);
                         tc_commit(&bars[FB_VE]);
                     }
@@ -243,21 +245,26 @@ __global__ void __launch_bounds__(192, 2)
                     alpha = ex2(m - m_new);                  // m = -inf gives 0
                 }
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                // P = exp2(s * scale*log2e - m), written over S as two packed bf16
+                // terms: P_hi = bf16(P) in columns [0, 64) and P_lo = bf16(P - P_hi)
+                // in columns [64, 128).  O accumulates P_hi V + P_lo V, so O carries
+                // ~16 significant bits of P instead of one bf16 rounding (the
+                // backward's D = rowsum(dO * O) depends on that accuracy).
                 float sum0 = 0.f, sum1 = 0.f;
-                // P = exp2(s * scale*log2e - m) as packed bf16, written over S in
-                // two 32-column chunks (S is already in registers).
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    uint32_t pk[32];
+                for (int hh = 0; hh < 4; ++hh) {
+                    uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float p0 = ex2(fmaf(sv[hh * 64 + 2 * c], a.scale_log2, -m_use));
-                        const float p1 = ex2(fmaf(sv[hh * 64 + 2 * c + 1], a.scale_log2, -m_use));
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ex2(fmaf(sv[hh * 32 + 2 * c], a.scale_log2, -m_use));
+                        const float p1 = ex2(fmaf(sv[hh * 32 + 2 * c + 1], a.scale_log2, -m_use));
                         sum0 += p0;
                         sum1 += p1;
-                        pk[c] = pack_bf16x2(p0, p1);
+                        hi[c] = pack_bf16x2(p0, p1);
+                        lo[c] = pack_bf16x2(p0 - __uint_as_float(hi[c] << 16), p1 - __uint_as_float(hi[c] & 0xffff0000u));
                     }
-                    tmem_st32(tS + lane_off + hh * 32, pk);
+                    tmem_st16(tS + lane_off + hh * 16, hi);
+                    tmem_st16(tS + lane_off + 64 + hh * 16, lo);
                 }
                 l = l * alpha + (sum0 + sum1);
                 m = m_new;

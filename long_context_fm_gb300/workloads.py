@@ -243,10 +243,3 @@ def make_inputs(wl: Workload, seed: int = 0, device="cpu", need_do: bool = True)
             t.mul_(wl.input_scale)
         out.append(t.to(torch.bfloat16))
     return tuple(out)
-
-
-def head_shards(n_units: int, world: int, rank: int):
-    """Contiguous split of ``n_units`` independent (batch, head) units over ranks."""
-    base, extra = divmod(n_units, world)
-    start = rank * base + min(rank, extra)
-    return start, start + base + (1 if rank < extra else 0)

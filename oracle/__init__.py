@@ -42,7 +42,12 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    lib = ctypes.CDLL(build())
+    _lib = _configure(ctypes.CDLL(build()))
+    return _lib
+
+
+def _configure(lib):
+    """Declare the C signatures on a loaded copy of the oracle library."""
     P = ctypes.c_void_p
     I64 = ctypes.c_int64
     lib.oracle_dense_from_cols.argtypes = [P, P, P, P, I64, P]
@@ -58,7 +63,6 @@ def _load():
     lib.oracle_tile_labels.argtypes = [P, P, P, P, I64, ctypes.c_int, ctypes.c_int, P]
     lib.oracle_tile_labels_exact.argtypes = [P, P, P, P, I64, ctypes.c_int, ctypes.c_int, P]
     lib.oracle_num_threads.restype = ctypes.c_int
-    _lib = lib
     return lib
 
 

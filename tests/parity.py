@@ -27,6 +27,24 @@ def check_close(name, got, ref, atol=ATOL, rl2=RTOL_L2):
     return err, rel
 
 
+def check_all(items):
+    """check_close on every (name, got, ref) and the lse check on ("lse", got, ref);
+    every output is checked and all failures are reported together."""
+    msgs, report = [], []
+    for name, got, ref in items:
+        try:
+            if name == "lse":
+                check_lse(got, ref)
+                report.append("lse ok")
+            else:
+                err, rel = check_close(name, got, ref)
+                report.append(f"{name} {err:.2e}/{rel:.2e}")
+        except AssertionError as e:
+            msgs.append(str(e))
+    print("; ".join(report))
+    assert not msgs, " | ".join(msgs)
+
+
 def check_lse(got, ref):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

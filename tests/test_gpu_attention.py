@@ -6,7 +6,7 @@ import torch
 
 import oracle
 from long_context_fm_gb300 import workloads as W
-from parity import check_close, check_lse, run_fm
+from parity import check_all, check_close, check_lse, run_fm
 
 pytestmark = pytest.mark.gpu
 
@@ -25,11 +25,9 @@ def test_fwd_bwd_match_oracle(fm, name):
     out = run_fm(fm, wl, m, q, k, v, dO)
     O, L = oracle.forward(q, k, v, m, wl.scale)
     g = oracle.backward(q, k, v, dO, m, wl.scale)
-    check_close("O", out["o"].cpu().numpy(), O)
-    check_lse(out["lse"].cpu().numpy(), L)
-    check_close("dQ", out["dq"].cpu().numpy(), g["dq"])
-    check_close("dK", out["dk"].cpu().numpy(), g["dk"])
-    check_close("dV", out["dv"].cpu().numpy(), g["dv"])
+    check_all([("O", out["o"].cpu().numpy(), O), ("lse", out["lse"].cpu().numpy(), L),
+               ("dQ", out["dq"].cpu().numpy(), g["dq"]), ("dK", out["dk"].cpu().numpy(), g["dk"]),
+               ("dV", out["dv"].cpu().numpy(), g["dv"])])
 
 
 @pytest.mark.parametrize("name", ["docs_small", "random_cols_d64", "causal_ragged"])

@@ -299,3 +299,25 @@ def test_softmax_max_subtraction_identity():
     s = 0.5 * (q[0, 0].double() @ k[0, 0].double().T).numpy()
     naive = np.log(np.array([np.exp(s[i, : i + 1]).sum() for i in range(N)]))
     np.testing.assert_allclose(lse[0, 0], naive, rtol=1e-13)
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("which", ["lower", "upper"])
+def test_labels_sound_with_one_random_range_per_column(seed, which):
+    """Only one of the two ranges used, with random starts and ends: the rule
+    must still never call a tile SKIP or FULL wrongly, and it must find some
+    SKIP and FULL tiles (narrow random ranges leave whole tiles untouched)."""
+    rng = np.random.default_rng(500 + seed)
+    N = 700
+    a = rng.integers(0, N + 1, size=N)
+    w = rng.integers(0, 200, size=N)
+    s0 = np.sort(a).astype(np.int32)                    # starts grow with the column
+    e0 = np.minimum(s0 + w, N).astype(np.int32)
+    empty_lo = (np.full(N, N, np.int32), np.full(N, N, np.int32))
+    empty_up = (np.zeros(N, np.int32), np.zeros(N, np.int32))
+    b = (s0, e0) + empty_up if which == "lower" else empty_lo + (s0, e0)
+    for bq, bk in ((64, 64), (128, 128), (64, 128)):
+        lbl = oracle.tile_labels(*b, bq, bk)
+        ex = oracle.tile_labels(*b, bq, bk, exact=True)
+        assert np.all(ex[lbl == 0] == 0) and np.all(ex[lbl == 1] == 1)
+        assert (lbl == 1).any()
