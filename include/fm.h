@@ -164,6 +164,31 @@ FM_API fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const 
                       fm_stream_t stream);
 
 /*
+ * fm_attn_bwd_noalloc — DEVICE, async.  No counterpart in the paper: this
+ * entry point exists for callers that may not allocate device memory (code
+ * running under another framework's allocator, latency-critical loops that
+ * must not call cudaMalloc after start-up, plugins handed only their input
+ * and output buffers).  Same contract and results as fm_attn_bwd, but the
+ * workspace comes from a fixed array inside the library instead of the
+ * caller, so nothing is allocated.
+ * Limit: fm_bwd_workspace_bytes(B, H, N, d) <= FM_NOALLOC_SCRATCH_BYTES
+ * (64 MiB: about 130,000 rows B*H*N at d = 128); larger sizes return
+ * FM_ERR_WORKSPACE before anything is launched.
+ * The first call made with a device current looks up the array's device
+ * address on that device; make that first call before any stream capture.
+ * A device that has loaded the array keeps it until the process exits.
+ * Every call uses the same array: calls whose work overlaps on the GPU (for
+ * example on two streams) race and give wrong results; calls ordered on one
+ * stream are safe.  Each call clears what it needs; nothing carries over.
+ */
+#define FM_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+FM_API fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                     int o_dtype, const float *lse, const void *dO, fm_bounds m,
+                                     const void *plan, int B, int H, int N, int d, float scale,
+                                     void *dq, void *dk, void *dv, int grad_dtype,
+                                     int32_t *dev_status, fm_stream_t stream);
+
+/*
  * Per-kernel timing (the library's own tracing).  fm_profile_begin starts
  * recording a CUDA event pair around every kernel the library launches
  * (process-wide, up to 4096 launches); fm_profile_end waits for those

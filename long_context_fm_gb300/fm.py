@@ -26,7 +26,10 @@ KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "b
 
 EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_plan_bytes",
             "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
-            "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout"]
+            "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
+            "fm_attn_bwd_noalloc"]
+# Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class FmError(RuntimeError):
@@ -60,6 +63,8 @@ _lib.fm_bwd_workspace_bytes.restype = _SZ
 _lib.fm_bwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
 _lib.fm_attn_bwd.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _P, _P,
                              _I, _P, _SZ, _P, _P]
+_lib.fm_attn_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P,
+                                     _P, _P, _I, _P, _P]
 _lib.fm_profile_begin.argtypes = []
 _lib.fm_profile_end.restype = _I
 _lib.fm_profile_end.argtypes = [_P, _I]
@@ -188,6 +193,27 @@ def fm_attn_bwd(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk, dv, ws
                             _ptr(plan), B, H, N, d, float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
                             _dt(dq), _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
     _check(code, "fm_attn_bwd")
+
+
+def fm_attn_bwd_noalloc(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk, dv, dev_status,
+                        stream=None):
+    """fm_attn_bwd without a caller workspace: for callers that cannot
+    allocate device memory; the library's fixed built-in array is used
+    instead (see fm.h for the size limit and the rules on overlapping calls)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _dev(t, torch.bfloat16, n)
+    B, H, N, d = q.shape
+    for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _dev(t, t.dtype, n)
+        if t.shape != q.shape:
+            raise ValueError(f"{n} must have the shape of q")
+    if not (dq.dtype == dk.dtype == dv.dtype):
+        raise TypeError("dq, dk, dv must share one dtype")
+    _dev(lse, torch.float32, "lse")
+    code = _lib.fm_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(lse), _ptr(dO),
+                                    bounds, _ptr(plan), B, H, N, d, float(scale), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _dt(dq), _ptr(dev_status), _stream(stream))
+    _check(code, "fm_attn_bwd_noalloc")
 
 
 def fm_profile_begin():
