@@ -325,6 +325,7 @@ def main():
             "config": {"workload": r["wl"].name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
                        "mask": "log-normal documents (median 4096, sigma 1, clip [256, 32768]), causal within document",
                        "attended_pairs": r["pairs"], "outputs": "fp32 O, dQ, dK, dV",
+                       "precision": "standard (bf16 P and dS tensor-core operands, fp32 accumulation)",
                        "l2": "inputs larger than L2 (Q, K, V, dO 1 GiB), no flush"},
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "frac_of_peak": {"fwd": fwd_tflops / peak_burst, "fwd_bwd": value / world / peak_sus,

@@ -63,6 +63,17 @@ typedef enum {
 enum { FM_TILE_SKIP = 0, FM_TILE_FULL = 1, FM_TILE_PARTIAL = 2 };
 enum { FM_DT_BF16 = 0, FM_DT_F32 = 1 };
 
+/* Flags of fm_attn_fwd / fm_attn_bwd.
+ * FM_FLAG_PRECISE: the softmax probabilities P (forward and backward) and dS
+ * (backward) enter the tensor-core products as two bf16 terms, x = hi + lo
+ * with hi = bf16(x), lo = bf16(x - hi), instead of one bf16 rounding.  The
+ * products keep ~16 significant bits of P and dS (more tensor-core work:
+ * 1.5x the forward PV product, 1.6x the backward products).  Without it the
+ * kernels use the usual FlashAttention arithmetic (bf16 P and dS operands,
+ * fp32 accumulation).  Use it when gradients are large (|dQ| of tens), where
+ * one bf16 rounding of dS and of O (through D) shows in the result. */
+enum { FM_FLAG_PRECISE = 1 };
+
 /* Same type as cudaStream_t, so a cudaStream_t can be passed directly. */
 typedef struct CUstream_st *fm_stream_t;
 
@@ -135,11 +146,13 @@ FM_API size_t fm_fwd_workspace_bytes(int B, int H, int N, int d);
  * with O_i = 0 and lse_i = -inf for a row that attends nothing.
  * q, k, v: device bf16 [B, H, N, d]; plan from fm_tile_classify(m, 128, 128);
  * o: device [B, H, N, d] of o_dtype (FM_DT_BF16 / FM_DT_F32);
- * lse: device fp32 [B, H, N]; ws: fm_fwd_workspace_bytes() bytes or NULL.
+ * lse: device fp32 [B, H, N]; ws: fm_fwd_workspace_bytes() bytes or NULL;
+ * flags: 0 or FM_FLAG_PRECISE.
  */
 FM_API fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, const void *plan,
                       int B, int H, int N, int d, float scale, void *o, int o_dtype, float *lse,
-                      void *ws, size_t ws_bytes, int32_t *dev_status, fm_stream_t stream);
+                      void *ws, size_t ws_bytes, int flags, int32_t *dev_status,
+                      fm_stream_t stream);
 
 /* Workspace of fm_attn_bwd in bytes: fp32 dQ accumulator [B,H,N,d] plus
  * fp32 D = rowsum(dO * O) [B,H,N]. */
@@ -154,13 +167,14 @@ FM_API size_t fm_bwd_workspace_bytes(int B, int H, int N, int d);
  *     dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
  *     dQ = scale dS K,  dK = scale dS^T Q.
  * Same tile skipping as the forward.  o, lse: the forward's outputs (o of
- * o_dtype); dq, dk, dv: device [B, H, N, d] of grad_dtype; ws:
- * fm_bwd_workspace_bytes() bytes (overwritten).
+ * o_dtype); dq, dk, dv: device [B, H, N, d] of grad_dtype; flags: 0 or
+ * FM_FLAG_PRECISE (with a precise backward, compute O with a precise forward
+ * too: D is taken from O); ws: fm_bwd_workspace_bytes() bytes (overwritten).
  */
 FM_API fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o, int o_dtype,
                       const float *lse, const void *dO, fm_bounds m, const void *plan, int B,
                       int H, int N, int d, float scale, void *dq, void *dk, void *dv,
-                      int grad_dtype, void *ws, size_t ws_bytes, int32_t *dev_status,
+                      int grad_dtype, int flags, void *ws, size_t ws_bytes, int32_t *dev_status,
                       fm_stream_t stream);
 
 /*
@@ -185,7 +199,7 @@ FM_API fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const 
 FM_API fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                      int o_dtype, const float *lse, const void *dO, fm_bounds m,
                                      const void *plan, int B, int H, int N, int d, float scale,
-                                     void *dq, void *dk, void *dv, int grad_dtype,
+                                     void *dq, void *dk, void *dv, int grad_dtype, int flags,
                                      int32_t *dev_status, fm_stream_t stream);
 
 /*

@@ -8,13 +8,16 @@
 // arithmetic, only partial pairs evaluate the column-interval predicate.
 //
 // Main kernel: one CTA = one (b, h, 128-row KV tile); it walks the plan's
-// list of non-skip Q tiles of that KV tile, each as two 64-row halves.
+// list of non-skip Q tiles of that KV tile (staged in shared memory), each as
+// two 64-row halves.
 //   warp 0      TMA producer (K and V once; Q, dO halves double-buffered;
 //               lse and D staged into shared memory by the whole warp)
 //   warp 1      TMEM allocation; one thread issues the tcgen05 MMAs
-//   warps 2-5   one thread per KV row j: P^T and dS^T for the half
-//   warps 6-9   one thread per head-dim index: drains dQ^T from TMEM and adds
-//               it into the fp32 dQ accumulator (coalesced red.global.add)
+//   warps 2-9   two warpgroups, one thread per KV row j each: P^T and dS^T
+//               for columns [0, 32) and [32, 64) of the half
+//   warps 10-13 one thread per head-dim index: drain dQ^T from TMEM into the
+//               fp32 dQ accumulator (standard mode: shared-memory tile plus a
+//               bulk tensor reduce-add; precise mode: red.global.add)
 // TMEM (512 columns): dK [0, d), dV [128, 128 + d), S^T [256, 320),
 // dP^T [320, 384), dQ^T [384, 448).  Per half (M = 128 KV rows):
 //   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
@@ -95,7 +98,7 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, v
 }
 
 // ---------------------------------------------------------------- main kernel
-template <int D>
+template <int D, bool PRECISE>
 struct BwdSmem {
     static constexpr int kKBox = 128 * 128;     // 64 columns x 128 rows
     static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
@@ -103,13 +106,16 @@ struct BwdSmem {
     static constexpr int kQTile = 64 * D * 2;
     static constexpr int kOp = 128 * 128;       // one 128 x 64 bf16 operand tile
     static constexpr int kK = 0, kV = kKTile;
-    static constexpr int kQ = 2 * kKTile;                 // [2] stages
-    static constexpr int kdO = kQ + 2 * kQTile;           // [2] stages
-    static constexpr int kP = kdO + 2 * kQTile;           // P^T  high part
-    static constexpr int kPlo = kP + kOp;                 // P^T  low part
-    static constexpr int kdS = kPlo + kOp;                // dS^T high part
-    static constexpr int kdSlo = kdS + kOp;               // dS^T low part
-    static constexpr int kStat = kdSlo + kOp;             // lse2 [2][64], D [2][64]
+    static constexpr int kQ = 2 * kKTile;                   // [2] stages
+    static constexpr int kdO = kQ + 2 * kQTile;             // [2] stages
+    static constexpr int kP = kdO + 2 * kQTile;             // P^T  (high part)
+    static constexpr int kdS = kP + kOp;                    // dS^T (high part)
+    static constexpr int kPlo = kdS + kOp;                  // precise: P^T low part
+    static constexpr int kdSlo = kPlo + kOp;                // precise: dS^T low part
+    static constexpr int kDQ = PRECISE ? kdSlo + kOp : kPlo; // standard: fp32 dQ tile [64][D]
+    static constexpr int kList = PRECISE ? kDQ : kDQ + 64 * D * 4;
+    static constexpr int kListCap = 2048;                   // Q tiles staged from the plan
+    static constexpr int kStat = kList + kListCap * 4;      // lse2 [2][64], D [2][64]
     static constexpr int kBar = kStat + 4 * 64 * 4;
     static constexpr int kNumBar = 16;
     static constexpr int kMisc = kBar + kNumBar * 8;
@@ -119,7 +125,7 @@ struct BwdSmem {
 
 enum {
     BB_KV = 0, BB_QF0, BB_QF1, BB_QE0, BB_QE1, BB_SF, BB_SE, BB_PF, BB_DSE, BB_DQF, BB_DQE, BB_ACC,
-    BB_DRAIN
+    BB_DRAIN, BB_STF, BB_STE
 };
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
@@ -131,20 +137,35 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
     lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
 }
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+// Bulk reduce-add of a row-major fp32 shared-memory tile into global memory
+// through a tensor map (no multicast); completion tracked by a bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+template <int D, bool PRECISE>
+__global__ void __launch_bounds__(448, 1)
     fm_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const BwdArgs a)
+                  const __grid_constant__ CUtensorMap tdq, const BwdArgs a)
 {
-    using S = BwdSmem<D>;
+    using S = BwdSmem<D, PRECISE>;
     constexpr int NBOX = D / 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
     uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
-    uint8_t *sP = smem + S::kP, *sPlo = smem + S::kPlo, *sdS = smem + S::kdS, *sdSlo = smem + S::kdSlo;
+    uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS, *sPlo = smem + S::kPlo, *sdSlo = smem + S::kdSlo;
+    float *sDQ = reinterpret_cast<float *>(smem + S::kDQ);
+    int32_t *sList = reinterpret_cast<int32_t *>(smem + S::kList);
     float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [2][64]
     float *sD = sLse + 128;                                          // [2][64]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
@@ -170,18 +191,20 @@ __global__ void __launch_bounds__(320, 1)
         *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)sidx * L.n_k + kt] : 0;
         *abort = 0;
         mbar_init(&bars[BB_KV], 1);
-        mbar_init(&bars[BB_QF0], 32);
-        mbar_init(&bars[BB_QF1], 32);
+        mbar_init(&bars[BB_QF0], 33);
+        mbar_init(&bars[BB_QF1], 33);
         mbar_init(&bars[BB_QE0], 1);
         mbar_init(&bars[BB_QE1], 1);
         mbar_init(&bars[BB_SF], 1);
-        mbar_init(&bars[BB_SE], 128);
-        mbar_init(&bars[BB_PF], 128);
+        mbar_init(&bars[BB_SE], 256);
+        mbar_init(&bars[BB_PF], 256);
         mbar_init(&bars[BB_DSE], 1);
         mbar_init(&bars[BB_DQF], 1);
         mbar_init(&bars[BB_DQE], 128);
         mbar_init(&bars[BB_ACC], 1);
         mbar_init(&bars[BB_DRAIN], 1);
+        mbar_init(&bars[BB_STF], 128);
+        mbar_init(&bars[BB_STE], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -194,12 +217,17 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tmem = *tmem_holder;
     const uint32_t tdK = tmem, tdV = tmem + 128, tS = tmem + 256, tdP = tmem + 320, tdQ = tmem + 384;
     const int cnt = *cnt_sh;
-    const int32_t *list =
+    const int32_t *glist =
         reinterpret_cast<const int32_t *>(a.plan + L.off_col_list) + ((int64_t)sidx * L.n_k + kt) * L.n_q;
+    // Stage the list of non-skip Q tiles into shared memory (one global read
+    // per entry instead of one per entry per role).
+    for (int i = threadIdx.x; i < cnt && i < S::kListCap; i += blockDim.x) sList[i] = glist[i];
+    __syncthreads();
+    auto entry = [&](int t) { return t < S::kListCap ? sList[t] : glist[t]; };
     // Flat iteration over 64-row halves of the listed Q tiles.  Only the last
     // Q tile can have a second half beyond N, and it is last in the list.
-    const int n_it = (cnt > 0 && (list[cnt - 1] & kTileMask) * 128 + 64 >= N) ? 2 * cnt - 1 : 2 * cnt;
-    auto q0_of = [&](int it) { return (list[it >> 1] & kTileMask) * 128 + (it & 1) * 64; };
+    const int n_it = (cnt > 0 && (entry(cnt - 1) & kTileMask) * 128 + 64 >= N) ? 2 * cnt - 1 : 2 * cnt;
+    auto q0_of = [&](int it) { return (entry(it >> 1) & kTileMask) * 128 + (it & 1) * 64; };
 
     if (*ok_sh) {
         if (warp == 0) {
@@ -218,19 +246,20 @@ __global__ void __launch_bounds__(320, 1)
             for (; it < n_it; ++it) {
                 const int q0 = q0_of(it);
                 const int st = it & 1;
-                if (it >= 2 && !warp_wait(&bars[BB_QE0 + st], ((it >> 1) - 1) & 1, abort, a.status)) break;
+                // lse and D of the half's rows, loaded before the stage wait so
+                // the global latency overlaps it; rows beyond N get P = 0.
+                float lv[2], dv[2];
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
-                    const int r = lane + rr * 32, qi = q0 + r;
-                    float l2 = INFINITY, dd = 0.f;     // rows beyond N: P = 0
+                    const int qi = q0 + lane + rr * 32;
+                    lv[rr] = INFINITY;
+                    dv[rr] = 0.f;
                     if (qi < N) {
-                        const float lv = a.lse[(int64_t)bh * N + qi];
-                        l2 = (lv == -INFINITY) ? INFINITY : lv * 1.4426950408889634f;
-                        dd = a.Dvec[(int64_t)bh * N + qi];
+                        lv[rr] = a.lse[(int64_t)bh * N + qi];
+                        dv[rr] = a.Dvec[(int64_t)bh * N + qi];
                     }
-                    sLse[st * 64 + r] = l2;
-                    sD[st * 64 + r] = dd;
                 }
+                if (it >= 2 && !warp_wait(&bars[BB_QE0 + st], ((it >> 1) - 1) & 1, abort, a.status)) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
 #pragma unroll
@@ -238,9 +267,14 @@ __global__ void __launch_bounds__(320, 1)
                         tma_load_3d(sQ + st * S::kQTile + x * S::kQBox, &tq, &bars[BB_QF0 + st], x * 64, q0, bh);
                         tma_load_3d(sdO + st * S::kQTile + x * S::kQBox, &tdo, &bars[BB_QF0 + st], x * 64, q0, bh);
                     }
-                } else {
-                    mbar_arrive(&bars[BB_QF0 + st]);
                 }
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = lane + rr * 32;
+                    sLse[st * 64 + r] = (lv[rr] == -INFINITY) ? INFINITY : lv[rr] * 1.4426950408889634f;
+                    sD[st * 64 + r] = dv[rr];
+                }
+                mbar_arrive(&bars[BB_QF0 + st]);     // 32 arrivals after the stores (+1 expect_tx)
             }
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
@@ -257,6 +291,7 @@ __global__ void __launch_bounds__(320, 1)
                 constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
                 constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
                 constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
+                constexpr int NPART = PRECISE ? 2 : 1;
                 const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
                 const uint32_t aP[2] = {smem_u32(sP), smem_u32(sPlo)};
                 const uint32_t adS[2] = {smem_u32(sdS), smem_u32(sdSlo)};
@@ -295,13 +330,13 @@ __global__ void __launch_bounds__(320, 1)
                     tc_fence_after();
                     const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
+                    for (int part = 0; part < NPART; ++part)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ss(tdV, sdesc_sw128(aP[part] + kk * 32, 16, 1024),
                                    sdesc_sw128(adO + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || part > 0 || kk > 0));
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
+                    for (int part = 0; part < NPART; ++part)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ss(tdK, sdesc_sw128(adS[part] + kk * 32, 16, 1024),
@@ -309,7 +344,7 @@ __global__ void __launch_bounds__(320, 1)
                     if (it > 0 && !mbar_wait(&bars[BB_DQE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
+                    for (int part = 0; part < NPART; ++part)
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_ss(tdQ, sdesc_sw128(aK + kk * 2048, S::kKBox, 1024),
@@ -324,10 +359,14 @@ __global__ void __launch_bounds__(320, 1)
                 tc_commit(&bars[BB_DRAIN]);
                 mbar_wait_drain(&bars[BB_DRAIN], 0, a.status);
             }
-        } else if (warp < 6) {
+        } else if (warp < 10) {
             // ------------------------------------------------ P^T / dS^T
+            // Two warpgroups: warps 2-5 take columns [0, 32) of each half,
+            // warps 6-9 columns [32, 64); thread = KV row (TMEM lane).
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;       // KV row within the tile
+            const int c0 = (warp < 6) ? 0 : 32;      // first column of this warpgroup
+            const bool first_wg = warp < 6;
             const int j = kb + r;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             int lo0 = 0, lolen = 0, up0 = 0, uplen = 0x7fffffff;   // beyond N: masked everywhere
@@ -338,113 +377,111 @@ __global__ void __launch_bounds__(320, 1)
             }
             const bool kv_tail = kb + 128 > N;
             bool ok = true;
-            int it = 0;
-            for (; it < n_it; ++it) {
+            for (int it = 0; it < n_it; ++it) {
                 const int q0 = q0_of(it);
-                const bool pred = ((list[it >> 1] >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
+                const bool pred = ((entry(it >> 1) >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
                 const int st = it & 1;
                 if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
                     !warp_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
                 tc_fence_after();
-                const float *l2 = sLse + st * 64;
-                const float *dd = sD + st * 64;
-                // P^T row: exp2(s * scale*log2e - lse*log2e), masked -> 0.
-                float p[64];
-                {
-                    uint32_t raw[2][32];
-                    tmem_ld32(tS + lane_off, raw[0]);
-                    tmem_ld32(tS + lane_off + 32, raw[1]);
-                    tmem_ld_wait();
-                    tmem_reg_fence(raw[0]);
-                    tmem_reg_fence(raw[1]);
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        float pv = ex2(fmaf(__uint_as_float(raw[c >> 5][c & 31]), a.scale_log2, -l2[c]));
-                        if (pred) {
-                            const int qi = q0 + c;
-                            const bool msk = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
-                                             ((unsigned)(qi - up0) < (unsigned)uplen);
-                            pv = msk ? 0.f : pv;
-                        }
-                        p[c] = pv;
-                    }
-                }
-                uint32_t draw[2][32];
-                tmem_ld32(tdP + lane_off, draw[0]);
-                tmem_ld32(tdP + lane_off + 32, draw[1]);
+                const float *l2 = sLse + st * 64 + c0;
+                const float *dd = sD + st * 64 + c0;
+                uint32_t sraw[32], draw[32];
+                tmem_ld32(tS + lane_off + c0, sraw);
+                tmem_ld32(tdP + lane_off + c0, draw);
                 tmem_ld_wait();
-                tmem_reg_fence(draw[0]);
-                tmem_reg_fence(draw[1]);
+                tmem_reg_fence(sraw);
+                tmem_reg_fence(draw);
                 tc_fence_before();
-                mbar_arrive(&bars[BB_SE]);      // S^T and dP^T may now be overwritten
+                mbar_arrive(&bars[BB_SE]);      // this warpgroup's half of S^T, dP^T is in registers
+                float p[32], ds[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float pv = ex2(fmaf(__uint_as_float(sraw[c]), a.scale_log2, -l2[c]));
+                    if (pred) {
+                        const int qi = q0 + c0 + c;
+                        const bool msk = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
+                                         ((unsigned)(qi - up0) < (unsigned)uplen);
+                        pv = msk ? 0.f : pv;
+                    }
+                    p[c] = pv;
+                    ds[c] = pv * (__uint_as_float(draw[c]) - dd[c]);
+                }
                 if (it > 0 && !warp_wait(&bars[BB_DSE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
                 // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
-                const int rowoff = r * 128;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int u = 0; u < 4; ++u) {
+                    const int chunk = (c0 >> 3) + u;
+                    const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
                     uint32_t ph[4], pl[4], dh[4], dl[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int c0 = 8 * c + 2 * u;
-                        const float ds0 = p[c0] * (__uint_as_float(draw[c0 >> 5][c0 & 31]) - dd[c0]);
-                        const float ds1 = p[c0 + 1] * (__uint_as_float(draw[(c0 + 1) >> 5][(c0 + 1) & 31]) - dd[c0 + 1]);
-                        split_bf16x2(p[c0], p[c0 + 1], ph[u], pl[u]);
-                        split_bf16x2(ds0, ds1, dh[u], dl[u]);
+                    for (int w2 = 0; w2 < 4; ++w2) {
+                        const int c = 8 * u + 2 * w2;
+                        if (PRECISE) {
+                            split_bf16x2(p[c], p[c + 1], ph[w2], pl[w2]);
+                            split_bf16x2(ds[c], ds[c + 1], dh[w2], dl[w2]);
+                        } else {
+                            ph[w2] = pack_bf16x2(p[c], p[c + 1]);
+                            dh[w2] = pack_bf16x2(ds[c], ds[c + 1]);
+                        }
                     }
-                    const int off = rowoff + ((c ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4 *>(sP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                    *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
                     *reinterpret_cast<uint4 *>(sdS + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-                    *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
+                    if (PRECISE) {
+                        *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                        *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
+                    }
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[BB_PF]);
             }
             // ------------------------------------------------ dK, dV epilogue
+            // The first warpgroup stores dK, the second dV.
             if (ok && (n_it == 0 || warp_wait(&bars[BB_ACC], 0, abort, a.status))) {
                 tc_fence_after();
                 const bool row_in = j < N;
                 const int64_t row = (int64_t)bh * N + j;
+                const uint32_t tsrc = first_wg ? tdK : tdV;
+                const float mul = first_wg ? a.scale : 1.f;
+                void *dst = first_wg ? a.dk : a.dv;
 #pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    const uint32_t tsrc = which == 0 ? tdK : tdV;
-                    const float mul = which == 0 ? a.scale : 1.f;
-                    void *dst = which == 0 ? a.dk : a.dv;
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    if (n_it > 0) {            // warp-uniform: every lane loads
+                        tmem_ld32(tsrc + lane_off + c * 32, v);
+                        tmem_ld_wait();
+                        tmem_reg_fence(v);
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t v[32];
-                        if (n_it > 0) {            // warp-uniform: every lane loads
-                            tmem_ld32(tsrc + lane_off + c * 32, v);
-                            tmem_ld_wait();
-                            tmem_reg_fence(v);
-                        } else {
+                        for (int u = 0; u < 32; ++u) v[u] = 0u;
+                    }
+                    if (!row_in) continue;
+                    if (a.g_f32) {
+                        float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + c * 32);
 #pragma unroll
-                            for (int u = 0; u < 32; ++u) v[u] = 0u;
-                        }
-                        if (!row_in) continue;
-                        if (a.g_f32) {
-                            float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + c * 32);
+                        for (int u = 0; u < 8; ++u)
+                            pp[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
+                                                __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
+                    } else {
+                        uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + c * 32);
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                pp[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
-                                                    __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
-                        } else {
-                            uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + c * 32);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                pp[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
-                                                   pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
-                                                   pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
-                                                   pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
-                        }
+                        for (int u = 0; u < 4; ++u)
+                            pp[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
+                                               pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
+                                               pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
+                                               pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
                     }
                 }
             }
         } else {
             // ------------------------------------------------ dQ drain
+            // Thread = head-dim index (TMEM lane of dQ^T).  Standard mode:
+            // the 64 x d tile goes through shared memory and one bulk
+            // reduce-add per half; precise mode: coalesced red.global.add.
             const int quarter = warp & 3;
-            const int dd = quarter * 32 + lane;      // head-dim index = TMEM lane of dQ^T
+            const int dd = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const bool leader = (warp == 10 && lane == 0);
             for (int it = 0; it < n_it; ++it) {
                 const int q0 = q0_of(it);
                 if (!warp_wait(&bars[BB_DQF], it & 1, abort, a.status)) break;
@@ -456,14 +493,34 @@ __global__ void __launch_bounds__(320, 1)
                 tmem_reg_fence(v[0]); tmem_reg_fence(v[1]);
                 tc_fence_before();
                 mbar_arrive(&bars[BB_DQE]);
-                if (dd < D) {
-                    float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
-                    const int lim = min(64, N - q0);
+                if (PRECISE) {
+                    if (dd < D) {
+                        float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
+                        const int lim = min(64, N - q0);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
+                        for (int c = 0; c < 64; ++c)
+                            if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
+                    }
+                } else {
+                    if (it > 0 && !warp_wait(&bars[BB_STE], (it - 1) & 1, abort, a.status)) break;
+                    if (dd < D) {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) sDQ[c * D + dd] = __uint_as_float(v[c >> 5][c & 31]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&bars[BB_STF]);
+                    if (leader) {
+                        // Rows beyond N are clipped by the tensor map.
+                        if (mbar_wait(&bars[BB_STF], it & 1, abort, a.status)) {
+                            tma_reduce_add_3d(&tdq, sDQ, 0, q0, bh);
+                            bulk_commit();
+                            bulk_wait_read0();
+                        }
+                        mbar_arrive(&bars[BB_STE]);
+                    }
                 }
             }
+            if (!PRECISE && leader) bulk_wait0();   // reductions complete before exit
         }
     }
     tc_fence_before();
@@ -493,24 +550,30 @@ fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dou
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
-fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const CUtensorMap &tdo, const BwdArgs &a, int d, cudaStream_t stream)
+template <int D, bool PRECISE>
+static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a,
+                            cudaStream_t stream)
 {
-    const dim3 grid(a.L.n_k, a.H, a.B);
-    if (d == 128) {
-        constexpr int smem = BwdSmem<128>::kBytes;
-        if (cudaFuncSetAttribute(fm_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return FM_ERR_CUDA;
-        ProfScope ps(kKBwd, stream);
-        fm_bwd_kernel<128><<<grid, 320, smem, stream>>>(tq, tk, tv, tdo, a);
-    } else {
-        constexpr int smem = BwdSmem<64>::kBytes;
-        if (cudaFuncSetAttribute(fm_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return FM_ERR_CUDA;
-        ProfScope ps(kKBwd, stream);
-        fm_bwd_kernel<64><<<grid, 320, smem, stream>>>(tq, tk, tv, tdo, a);
-    }
+    constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    if (cudaFuncSetAttribute(fm_bwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return FM_ERR_CUDA;
+    ProfScope ps(kKBwd, stream);
+    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 448, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a, int d,
+                             bool precise, cudaStream_t stream)
+{
+    if (d == 128)
+        return precise ? launch_bwd<128, true>(tq, tk, tv, tdo, tdq, a, stream)
+                       : launch_bwd<128, false>(tq, tk, tv, tdo, tdq, a, stream);
+    return precise ? launch_bwd<64, true>(tq, tk, tv, tdo, tdq, a, stream)
+                   : launch_bwd<64, false>(tq, tk, tv, tdo, tdq, a, stream);
 }
 
 fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,

@@ -7,21 +7,29 @@
 // §4.1 items 1-3 (bounds staged in shared memory, skip decided before the KV
 // block is loaded, mask fused into the softmax).
 //
-// One CTA = one (b, h, 128-row Q tile).  Roles:
-//   warp 0      TMA producer: Q once, then K and V of each non-skip KV tile
-//               from the plan's ordered list (skip tiles are never loaded);
-//   warp 1      allocates TMEM, one thread issues the tcgen05 MMAs;
-//   warps 2-5   softmax, one thread per Q row = TMEM lane.
-// TMEM (256 columns): S = Q K^T at columns [0, 128) (fp32), then overwritten
-// in place by P as two packed-bf16 terms (P_hi, P_lo: 64 columns each), the A
-// operands of O += P_hi V + P_lo V; O accumulates at columns [128, 128 + d).
+// One CTA = one (b, h) and two consecutive 128-row Q tiles (Q0, Q1) that
+// share every K/V load.  The CTA walks the union of the two tiles' lists of
+// non-skip KV tiles (from the plan, staged in shared memory); a KV tile that
+// only one Q tile needs is multiplied only for that tile, and skip tiles are
+// never loaded.  Roles:
+//   warp 0      TMA producer: Q0, Q1 once; K and V through a two-stage ring;
+//               the column bounds of partial tiles into shared memory
+//   warp 1      allocates TMEM; one thread issues the tcgen05 MMAs
+//   warps 2-5   softmax of Q0, one thread per row = TMEM lane
+//   warps 6-9   softmax of Q1
+// TMEM (512 columns): S0, S1 = Qi K^T at [0, 128) and [128, 256), each
+// overwritten in place by P as packed bf16 (the A operand of Oi += P V; in
+// precise mode a second term P_lo = bf16(P - bf16(P)) follows in the upper
+// 64 columns and Oi += P_hi V + P_lo V); O0, O1 accumulate at [256, 384) and
+// [384, 512).  The two softmax warpgroups ping-pong: while one works on its
+// scores the tensor core runs the other tile's products.
 // Online softmax in the base-2 domain with a lazy rescale: O and l are
 // rescaled only when the row max grows by more than 2^8, which keeps every
 // P <= 256 and leaves the final O / l unchanged.
-// Two CTAs share an SM (about 100 KB shared memory and 256 TMEM columns each)
-// so one CTA's softmax overlaps the other's MMAs.
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <climits>
 
 #include "fm_internal.h"
 #include "fm_ptx.cuh"
@@ -31,22 +39,50 @@ namespace fm {
 template <int D>
 struct FwdSmem {
     static constexpr int kBox = 128 * 128;        // one 64-column, 128-row bf16 box
-    static constexpr int kTile = 128 * D * 2;     // Q, K or V tile
-    static constexpr int kQ = 0, kK = kTile, kV = 2 * kTile;
-    static constexpr int kBnd = 3 * kTile;        // int4 [2][128]
-    static constexpr int kBar = kBnd + 4096;
-    static constexpr int kNumBar = 10;
+    static constexpr int kTile = 128 * D * 2;     // one Q, K or V tile
+    static constexpr int kQ0 = 0, kQ1 = kTile;
+    static constexpr int kK = 2 * kTile;          // [2] stages
+    static constexpr int kV = 4 * kTile;          // [2] stages
+    static constexpr int kBnd = 6 * kTile;        // int4 [2][128]
+    static constexpr int kListCap = 2048;         // KV tiles per Q tile staged from the plan
+    static constexpr int kList0 = kBnd + 4096;
+    static constexpr int kList1 = kList0 + kListCap * 4;
+    static constexpr int kBar = kList1 + kListCap * 4;
+    static constexpr int kNumBar = 20;
     static constexpr int kMisc = kBar + kNumBar * 8;
-    static constexpr int kUsed = kMisc + 64;
-    // Request at least 100 KB so that no more than two CTAs (2 x 256 TMEM
-    // columns) are resident on one SM.
-    static constexpr int kBytes = (kUsed + 1024 > 100 * 1024) ? kUsed + 1024 : 100 * 1024;
+    // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
+    static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
 };
 
-enum { FB_Q = 0, FB_K, FB_V, FB_KE, FB_VE, FB_S, FB_P, FB_O, FB_DRAIN, FB_BND };
+enum {
+    FB_Q = 0, FB_KF0, FB_KF1, FB_KE0, FB_KE1, FB_VF0, FB_VF1, FB_VE0, FB_VE1, FB_BF0, FB_BF1,
+    FB_S0, FB_S1, FB_P0, FB_P1, FB_O0, FB_O1, FB_DRAIN
+};
 
-template <int D>
-__global__ void __launch_bounds__(192, 2)
+// Walks the union of two ascending lists of KV tiles (entries tile | label << 28).
+struct TileMerge {
+    const int32_t *s0, *s1, *g0, *g1;
+    int n0, n1, i0, i1, cap;
+    __device__ __forceinline__ int32_t at0(int i) const { return i < cap ? s0[i] : g0[i]; }
+    __device__ __forceinline__ int32_t at1(int i) const { return i < cap ? s1[i] : g1[i]; }
+    // kt: next KV tile; lab0 / lab1: its label for Q0 / Q1, or -1 if that
+    // Q tile skips it.
+    __device__ __forceinline__ bool next(int &kt, int &lab0, int &lab1)
+    {
+        if (i0 >= n0 && i1 >= n1) return false;
+        const int32_t e0 = i0 < n0 ? at0(i0) : INT_MAX, e1 = i1 < n1 ? at1(i1) : INT_MAX;
+        const int k0 = i0 < n0 ? (e0 & kTileMask) : INT_MAX, k1 = i1 < n1 ? (e1 & kTileMask) : INT_MAX;
+        kt = min(k0, k1);
+        lab0 = -1;
+        lab1 = -1;
+        if (k0 == kt) { lab0 = e0 >> kLabelShift; ++i0; }
+        if (k1 == kt) { lab1 = e1 >> kLabelShift; ++i1; }
+        return true;
+    }
+};
+
+template <int D, bool PRECISE>
+__global__ void __launch_bounds__(320, 1)
     fm_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a)
 {
@@ -55,17 +91,20 @@ __global__ void __launch_bounds__(192, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *sQ = smem + S::kQ, *sK = smem + S::kK, *sV = smem + S::kV;
     int4 *sBnd = reinterpret_cast<int4 *>(smem + S::kBnd);
+    int32_t *sList0 = reinterpret_cast<int32_t *>(smem + S::kList0);
+    int32_t *sList1 = reinterpret_cast<int32_t *>(smem + S::kList1);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
-    int *cnt_sh = reinterpret_cast<int *>(smem + S::kMisc + 8);
-    int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
+    int *cnt_sh = reinterpret_cast<int *>(smem + S::kMisc + 8);   // [2]
+    int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 16);
 
     const int warp = warp_id(), lane = lane_id();
     const PlanLayout &L = a.L;
-    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;   // heavy causal tiles first
+    const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;   // heavy causal tiles first
+    const int qt0 = 2 * pair;
+    const bool has1 = qt0 + 1 < L.n_q;
     const int h = blockIdx.y, b = blockIdx.z;
     const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
     const int bh = b * a.H + h;
@@ -77,251 +116,309 @@ __global__ void __launch_bounds__(192, 2)
                         ph->bq == 128 && ph->bk == 128;
         if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
         *ok_sh = ok;
-        *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_row_cnt)[(int64_t)sidx * L.n_q + qt] : 0;
+        const int32_t *rc = reinterpret_cast<const int32_t *>(a.plan + L.off_row_cnt) + (int64_t)sidx * L.n_q;
+        cnt_sh[0] = ok ? rc[qt0] : 0;
+        cnt_sh[1] = (ok && has1) ? rc[qt0 + 1] : 0;
         *abort = 0;
         mbar_init(&bars[FB_Q], 1);
-        mbar_init(&bars[FB_K], 1);
-        mbar_init(&bars[FB_V], 1);
-        mbar_init(&bars[FB_KE], 1);
-        mbar_init(&bars[FB_VE], 1);
-        mbar_init(&bars[FB_S], 1);
-        mbar_init(&bars[FB_P], 128);
-        mbar_init(&bars[FB_O], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[FB_KF0 + s], 1);
+            mbar_init(&bars[FB_KE0 + s], 1);
+            mbar_init(&bars[FB_VF0 + s], 1);
+            mbar_init(&bars[FB_VE0 + s], 1);
+            mbar_init(&bars[FB_BF0 + s], 32);
+            mbar_init(&bars[FB_S0 + s], 1);
+            mbar_init(&bars[FB_P0 + s], 128);
+            mbar_init(&bars[FB_O0 + s], 1);
+        }
         mbar_init(&bars[FB_DRAIN], 1);
-        mbar_init(&bars[FB_BND], 128);
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_holder, 256);
+        tmem_alloc(tmem_holder, 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const uint32_t tS = tmem, tO = tmem + 128;
-    const int cnt = *cnt_sh;
-    const int32_t *list =
-        reinterpret_cast<const int32_t *>(a.plan + L.off_row_list) + ((int64_t)sidx * L.n_q + qt) * L.n_k;
+    const int n0 = cnt_sh[0], n1 = cnt_sh[1];
+    const int32_t *g0 =
+        reinterpret_cast<const int32_t *>(a.plan + L.off_row_list) + ((int64_t)sidx * L.n_q + qt0) * L.n_k;
+    const int32_t *g1 = g0 + L.n_k;
+    for (int i = threadIdx.x; i < S::kListCap; i += blockDim.x) {
+        if (i < n0) sList0[i] = g0[i];
+        if (i < n1) sList1[i] = g1[i];
+    }
+    __syncthreads();
+    TileMerge walk{sList0, sList1, g0, g1, n0, n1, 0, 0, S::kListCap};
+    const bool any = n0 + n1 > 0;
 
     if (*ok_sh) {
         if (warp == 0) {
             // ------------------------------------------------ TMA producer
-            if (lane == 0) {
+            if (lane == 0 && any) {
                 tma_prefetch_desc(&tq);
                 tma_prefetch_desc(&tk);
                 tma_prefetch_desc(&tv);
-                int issued = 0;
-                if (cnt > 0) {
-                    mbar_arrive_expect_tx(&bars[FB_Q], S::kTile);
+                mbar_arrive_expect_tx(&bars[FB_Q], (has1 ? 2 : 1) * S::kTile);
 #pragma unroll
-                    for (int x = 0; x < NBOX; ++x)
-                        tma_load_3d(sQ + x * S::kBox, &tq, &bars[FB_Q], x * 64, qt * 128, bh);
+                for (int x = 0; x < NBOX; ++x) {
+                    tma_load_3d(smem + S::kQ0 + x * S::kBox, &tq, &bars[FB_Q], x * 64, qt0 * 128, bh);
+                    if (has1) tma_load_3d(smem + S::kQ1 + x * S::kBox, &tq, &bars[FB_Q], x * 64, qt0 * 128 + 128, bh);
                 }
-                for (int t = 0; t < cnt; ++t) {
-                    const int kt = list[t] & kTileMask;
-                    if (t > 0 && !mbar_wait(&bars[FB_KE], (t - 1) & 1, abort, a.status)) break;
-                    mbar_arrive_expect_tx(&bars[FB_K], S::kTile);
+            }
+            int t = 0, kt, l0, l1;
+            for (; walk.next(kt, l0, l1); ++t) {
+                const int st = t & 1;
+                const uint32_t ph = ((t >> 1) - 1) & 1;
+                const int kb = kt * 128;
+                const bool pred = l0 == FM_TILE_PARTIAL || l1 == FM_TILE_PARTIAL || kb + 128 > N;
+                // Column bounds of a partial tile, loaded before the waits below so
+                // their latency overlaps them; stored as (start, length) pairs,
+                // columns beyond N masked for every row.
+                int4 bv[4];
+                if (pred) {
 #pragma unroll
-                    for (int x = 0; x < NBOX; ++x)
-                        tma_load_3d(sK + x * S::kBox, &tk, &bars[FB_K], x * 64, kt * 128, bh);
-                    if (t > 0 && !mbar_wait(&bars[FB_VE], (t - 1) & 1, abort, a.status)) {
-                        issued = -(t + 1);   // K of tile t in flight, V not
-                        break;
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = kb + lane * 4 + u;
+                        bv[u] = make_int4(0, 0, 0, 0x7fffffff);
+                        if (j < N) {
+                            const int64_t o = (int64_t)sidx * N + j;
+                            bv[u] = make_int4(a.lts[o], a.lte[o], a.uts[o], a.ute[o]);
+                        }
                     }
-                    mbar_arrive_expect_tx(&bars[FB_V], S::kTile);
+                }
+                if (t >= 2 && !warp_wait(&bars[FB_KE0 + st], ph, abort, a.status)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[FB_KF0 + st], S::kTile);
 #pragma unroll
                     for (int x = 0; x < NBOX; ++x)
-                        tma_load_3d(sV + x * S::kBox, &tv, &bars[FB_V], x * 64, kt * 128, bh);
-                    issued = t + 1;
+                        tma_load_3d(smem + S::kK + st * S::kTile + x * S::kBox, &tk, &bars[FB_KF0 + st], x * 64,
+                                    kb, bh);
                 }
-                // Drain: every issued copy must land before the CTA exits.
-                if (*abort) {
-                    const int nk = issued < 0 ? -issued : issued, nv = issued < 0 ? -issued - 1 : issued;
-                    if (cnt > 0) mbar_wait_drain(&bars[FB_Q], 0, a.status);
-                    if (nk > 0) mbar_wait_drain(&bars[FB_K], (nk - 1) & 1, a.status);
-                    if (nv > 0) mbar_wait_drain(&bars[FB_V], (nv - 1) & 1, a.status);
+                if (t >= 2 && !warp_wait(&bars[FB_VE0 + st], ph, abort, a.status)) {
+                    ++t;   // K of this tile is in flight
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[FB_VF0 + st], S::kTile);
+#pragma unroll
+                    for (int x = 0; x < NBOX; ++x)
+                        tma_load_3d(smem + S::kV + st * S::kTile + x * S::kBox, &tv, &bars[FB_VF0 + st], x * 64,
+                                    kb, bh);
+                }
+                if (pred) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int4 v = bv[u];
+                        sBnd[st * 128 + lane * 4 + u] = (kb + lane * 4 + u < N)
+                                                            ? make_int4(v.x, max(v.y - v.x, 0), v.z, max(v.w - v.z, 0))
+                                                            : v;
+                    }
+                }
+                mbar_arrive(&bars[FB_BF0 + st]);
+            }
+            // Drain copies still in flight (only possible after an abort).
+            if (lane == 0 && *abort) {
+                if (any) mbar_wait_drain(&bars[FB_Q], 0, a.status);
+                for (int k2 = (t > 2 ? t - 2 : 0); k2 < t; ++k2) {
+                    mbar_wait_drain(&bars[FB_KF0 + (k2 & 1)], (k2 >> 1) & 1, a.status);
+                    mbar_wait_drain(&bars[FB_VF0 + (k2 & 1)], (k2 >> 1) & 1, a.status);
                 }
             }
         } else if (warp == 1) {
             // ------------------------------------------------ MMA issuer
-            if (lane == 0) {
+            if (lane == 0 && any) {
                 constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
                 constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-                const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-                if (cnt > 0 && mbar_wait(&bars[FB_Q], 0, abort, a.status)) {
-                    for (int t = 0; t < cnt; ++t) {
-                        if (!mbar_wait(&bars[FB_K], t & 1, abort, a.status)) break;
-                        if (t > 0 && !mbar_wait(&bars[FB_O], (t - 1) & 1, abort, a.status)) break;
+                constexpr int NPART = PRECISE ? 2 : 1;
+                const uint32_t aQ[2] = {smem_u32(smem + S::kQ0), smem_u32(smem + S::kQ1)};
+                int c[2] = {0, 0};
+                bool ok = mbar_wait(&bars[FB_Q], 0, abort, a.status);
+                int t = 0, kt, lab[2];
+                for (; ok && walk.next(kt, lab[0], lab[1]); ++t) {
+                    const int st = t & 1;
+                    const uint32_t ph = (t >> 1) & 1;
+                    const uint32_t aK = smem_u32(smem + S::kK + st * S::kTile);
+                    const uint32_t aV = smem_u32(smem + S::kV + st * S::kTile);
+                    if (!mbar_wait(&bars[FB_KF0 + st], ph, abort, a.status)) { ok = false; break; }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        if (lab[q] < 0) continue;
+                        // S_q aliases P_q of the previous tile: wait for that PV.
+                        if (c[q] > 0 && !mbar_wait(&bars[FB_O0 + q], (c[q] - 1) & 1, abort, a.status)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * S::kBox + (kk & 3) * 32;
-                            mma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024),
-                                   idS, kk > 0);
+                            mma_ss(tmem + q * 128, sdesc_sw128(aQ[q] + off, 16, 1024),
+                                   sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
                         }
-                        tc_commit(&bars[FB_S]);
-                        tc_commit(&bars[FB_KE]);
-                        if (!mbar_wait(&bars[FB_P], t & 1, abort, a.status)) break;
-                        if (!mbar_wait(&bars[FB_V], t & 1, abort, a.status)) break;
+                        tc_commit(&bars[FB_S0 + q]);
+                    }
+                    if (!ok) break;
+                    tc_commit(&bars[FB_KE0 + st]);
+                    if (!mbar_wait(&bars[FB_VF0 + st], ph, abort, a.status)) { ok = false; break; }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        if (lab[q] < 0) continue;
+                        if (!mbar_wait(&bars[FB_P0 + q], c[q] & 1, abort, a.status)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
-                        for (int part = 0; part < 2; ++part)     // P_hi V, then P_lo V
+                        for (int part = 0; part < NPART; ++part)   // P_hi V (+ P_lo V)
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)
-                                mma_ts(tO, tS + part * 64 + kk * 8, sdesc_sw128(aV + kk * 2048, S::kBox, 1024),
-                                       idO, (t > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[FB_O]);
-                        tc_commit(&bars[FB_VE]);
+                                mma_ts(tmem + 256 + q * 128, tmem + q * 128 + part * 64 + kk * 8,
+                                       sdesc_sw128(aV + kk * 2048, S::kBox, 1024), idO, (c[q] > 0 || part > 0 || kk > 0));
+                        tc_commit(&bars[FB_O0 + q]);
+                        ++c[q];
                     }
+                    if (!ok) break;
+                    tc_commit(&bars[FB_VE0 + st]);
                 }
+            }
+            if (lane == 0) {
                 // Every MMA of this CTA completes before TMEM is released.
                 tc_commit(&bars[FB_DRAIN]);
                 mbar_wait_drain(&bars[FB_DRAIN], 0, a.status);
             }
         } else {
-            // ------------------------------------------------ softmax
+            // ------------------------------------------------ softmax (Q0: warps 2-5, Q1: warps 6-9)
+            const int q = (warp < 6) ? 0 : 1;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
-            const int i = qt * 128 + r;
+            const int i = (qt0 + q) * 128 + r;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-            float m = -INFINITY, l = 0.f;
-            int npart = 0;
+            const uint32_t tS = tmem + q * 128, tO = tmem + 256 + q * 128;
+            float m = -INFINITY, l = 0.f, lr = 0.f;
+            int cnt = 0;
             bool done = true;
-            for (int t = 0; t < cnt; ++t) {
-                const int32_t e = list[t];
-                const int kt = e & kTileMask, lab = e >> kLabelShift;
-                const int kb = kt * 128;
-                const bool pred = (lab == FM_TILE_PARTIAL) || (kb + 128 > N);
-                int4 *bnd = sBnd + (npart & 1) * 128;
-                if (pred) {
-                    const int j = kb + r;
-                    int4 v;
-                    if (j < N) {
-                        const int64_t o = (int64_t)sidx * N + j;
-                        const int l0 = a.lts[o], l1 = a.lte[o], u0 = a.uts[o], u1 = a.ute[o];
-                        v = make_int4(l0, max(l1 - l0, 0), u0, max(u1 - u0, 0));
-                    } else {
-                        v = make_int4(0, 0, 0, 0x7fffffff);   // beyond N: masked for every row
-                    }
-                    bnd[r] = v;
-                    mbar_arrive(&bars[FB_BND]);
-                    if (!warp_wait(&bars[FB_BND], npart & 1, abort, a.status)) { done = false; break; }
-                    ++npart;
-                }
-                if (!warp_wait(&bars[FB_S], t & 1, abort, a.status)) { done = false; break; }
+            int t = 0, kt, lab[2];
+            for (; walk.next(kt, lab[0], lab[1]); ++t) {
+                if (lab[q] < 0) continue;
+                const int st = t & 1;
+                const bool pred = (lab[q] == FM_TILE_PARTIAL) || (kt * 128 + 128 > N);
+                if (!warp_wait(&bars[FB_S0 + q], cnt & 1, abort, a.status)) { done = false; break; }
+                if (pred && !warp_wait(&bars[FB_BF0 + st], (t >> 1) & 1, abort, a.status)) { done = false; break; }
                 tc_fence_after();
                 uint32_t raw[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS + lane_off + c * 32, raw[c]);
+                for (int cc = 0; cc < 4; ++cc) tmem_ld32(tS + lane_off + cc * 32, raw[cc]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_reg_fence(raw[c]);
+                for (int cc = 0; cc < 4; ++cc) tmem_reg_fence(raw[cc]);
                 float sv[128];
 #pragma unroll
-                for (int c = 0; c < 128; ++c) sv[c] = __uint_as_float(raw[c >> 5][c & 31]);
+                for (int cc = 0; cc < 128; ++cc) sv[cc] = __uint_as_float(raw[cc >> 5][cc & 31]);
                 if (pred) {
+                    const int4 *bnd = sBnd + st * 128;
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const int4 x = bnd[c];
-                        const bool msk = ((unsigned)(i - x.x) < (unsigned)x.y) ||
-                                         ((unsigned)(i - x.z) < (unsigned)x.w);
-                        sv[c] = msk ? -INFINITY : sv[c];
+                    for (int cc = 0; cc < 128; ++cc) {
+                        const int4 x = bnd[cc];
+                        const bool msk = ((unsigned)(i - x.x) < (unsigned)x.y) || ((unsigned)(i - x.z) < (unsigned)x.w);
+                        sv[cc] = msk ? -INFINITY : sv[cc];
                     }
                 }
                 float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, sv[c]);
-                    mx1 = fmaxf(mx1, sv[c + 1]);
-                    mx2 = fmaxf(mx2, sv[c + 2]);
-                    mx3 = fmaxf(mx3, sv[c + 3]);
+                for (int cc = 4; cc < 128; cc += 4) {
+                    mx0 = fmaxf(mx0, sv[cc]);
+                    mx1 = fmaxf(mx1, sv[cc + 1]);
+                    mx2 = fmaxf(mx2, sv[cc + 2]);
+                    mx3 = fmaxf(mx3, sv[cc + 3]);
                 }
-                const float rowmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-                const float mx = rowmax * a.scale_log2;     // -inf stays -inf
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;   // -inf stays -inf
                 float m_new = m, alpha = 1.f;
                 if (mx > m + 8.f) {
                     m_new = mx;
                     alpha = ex2(m - m_new);                  // m = -inf gives 0
                 }
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                // P = exp2(s * scale*log2e - m), written over S as two packed bf16
-                // terms: P_hi = bf16(P) in columns [0, 64) and P_lo = bf16(P - P_hi)
-                // in columns [64, 128).  O accumulates P_hi V + P_lo V, so O carries
-                // ~16 significant bits of P instead of one bf16 rounding (the
-                // backward's D = rowsum(dO * O) depends on that accuracy).
-                float sum0 = 0.f, sum1 = 0.f;
+                // P = exp2(s * scale*log2e - m), written over S as packed bf16.
+                // Precise mode: two terms, P_hi = bf16(P) in columns [0, 64) and
+                // P_lo = bf16(P - P_hi) in columns [64, 128).  Standard mode:
+                // P_hi only, and O is normalised by the sum of the rounded P,
+                // i.e. of the weights the PV product really applied, so the
+                // normalised weights sum to one.  lse uses the fp32 sum.
+                float sum0 = 0.f, sum1 = 0.f, rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                     uint32_t hi[16], lo[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float p0 = ex2(fmaf(sv[hh * 32 + 2 * c], a.scale_log2, -m_use));
-                        const float p1 = ex2(fmaf(sv[hh * 32 + 2 * c + 1], a.scale_log2, -m_use));
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const float p0 = ex2(fmaf(sv[hh * 32 + 2 * cc], a.scale_log2, -m_use));
+                        const float p1 = ex2(fmaf(sv[hh * 32 + 2 * cc + 1], a.scale_log2, -m_use));
                         sum0 += p0;
                         sum1 += p1;
-                        hi[c] = pack_bf16x2(p0, p1);
-                        lo[c] = pack_bf16x2(p0 - __uint_as_float(hi[c] << 16), p1 - __uint_as_float(hi[c] & 0xffff0000u));
+                        hi[cc] = pack_bf16x2(p0, p1);
+                        if (PRECISE) {
+                            lo[cc] = pack_bf16x2(p0 - __uint_as_float(hi[cc] << 16),
+                                                 p1 - __uint_as_float(hi[cc] & 0xffff0000u));
+                        } else {
+                            rs0 += __uint_as_float(hi[cc] << 16);
+                            rs1 += __uint_as_float(hi[cc] & 0xffff0000u);
+                        }
                     }
                     tmem_st16(tS + lane_off + hh * 16, hi);
-                    tmem_st16(tS + lane_off + 64 + hh * 16, lo);
+                    if (PRECISE) tmem_st16(tS + lane_off + 64 + hh * 16, lo);
                 }
                 l = l * alpha + (sum0 + sum1);
+                if (!PRECISE) lr = lr * alpha + (rs0 + rs1);
                 m = m_new;
-                // Rescale O when the max moved (O holds tiles 0..t-1; the PV MMA
-                // of tile t is issued only after this thread's arrive below).
-                if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
+                // Rescale O when the max moved (O holds this tile's earlier KV
+                // tiles; their PV finished before this S was computed).
+                if (__any_sync(0xffffffffu, cnt > 0 && alpha != 1.f)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t ov[32];
-                        tmem_ld32(tO + lane_off + c * 32, ov);
+                        tmem_ld32(tO + lane_off + cc * 32, ov);
                         tmem_ld_wait();
                         tmem_reg_fence(ov);
 #pragma unroll
                         for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * alpha);
-                        tmem_st32(tO + lane_off + c * 32, ov);
+                        tmem_st32(tO + lane_off + cc * 32, ov);
                     }
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars[FB_P]);
+                mbar_arrive(&bars[FB_P0 + q]);
+                ++cnt;
             }
             // ------------------------------------------------ epilogue
-            if (done && (cnt == 0 || warp_wait(&bars[FB_O], (cnt - 1) & 1, abort, a.status))) {
+            const bool tile_exists = q == 0 || has1;
+            if (tile_exists && done && (cnt == 0 || warp_wait(&bars[FB_O0 + q], (cnt - 1) & 1, abort, a.status))) {
                 tc_fence_after();
-                const float inv = (l > 0.f) ? 1.f / l : 0.f;
+                const float nrm = PRECISE ? l : lr;
+                const float inv = (nrm > 0.f) ? 1.f / nrm : 0.f;
                 const bool row_in = i < N;
                 const int64_t row = (int64_t)bh * N + i;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t ov[32];
                     if (cnt > 0) {
-                        tmem_ld32(tO + lane_off + c * 32, ov);
+                        tmem_ld32(tO + lane_off + cc * 32, ov);
                         tmem_ld_wait();
                         tmem_reg_fence(ov);
                     } else {
 #pragma unroll
                         for (int u = 0; u < 32; ++u) ov[u] = 0u;
                     }
-                    if (row_in) {
-                        if (a.o_f32) {
-                            float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + row * D + c * 32);
+                    if (!row_in) continue;
+                    if (a.o_f32) {
+                        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + row * D + cc * 32);
 #pragma unroll
-                            for (int u = 0; u < 8; ++u)
-                                dst[u] = make_float4(__uint_as_float(ov[4 * u]) * inv, __uint_as_float(ov[4 * u + 1]) * inv,
-                                                     __uint_as_float(ov[4 * u + 2]) * inv, __uint_as_float(ov[4 * u + 3]) * inv);
-                        } else {
-                            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + row * D + c * 32);
+                        for (int u = 0; u < 8; ++u)
+                            dst[u] = make_float4(__uint_as_float(ov[4 * u]) * inv, __uint_as_float(ov[4 * u + 1]) * inv,
+                                                 __uint_as_float(ov[4 * u + 2]) * inv, __uint_as_float(ov[4 * u + 3]) * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + row * D + cc * 32);
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                uint4 w;
-                                w.x = pack_bf16x2(__uint_as_float(ov[8 * u + 0]) * inv, __uint_as_float(ov[8 * u + 1]) * inv);
-                                w.y = pack_bf16x2(__uint_as_float(ov[8 * u + 2]) * inv, __uint_as_float(ov[8 * u + 3]) * inv);
-                                w.z = pack_bf16x2(__uint_as_float(ov[8 * u + 4]) * inv, __uint_as_float(ov[8 * u + 5]) * inv);
-                                w.w = pack_bf16x2(__uint_as_float(ov[8 * u + 6]) * inv, __uint_as_float(ov[8 * u + 7]) * inv);
-                                dst[u] = w;
-                            }
-                        }
+                        for (int u = 0; u < 4; ++u)
+                            dst[u] = make_uint4(pack_bf16x2(__uint_as_float(ov[8 * u + 0]) * inv, __uint_as_float(ov[8 * u + 1]) * inv),
+                                                pack_bf16x2(__uint_as_float(ov[8 * u + 2]) * inv, __uint_as_float(ov[8 * u + 3]) * inv),
+                                                pack_bf16x2(__uint_as_float(ov[8 * u + 4]) * inv, __uint_as_float(ov[8 * u + 5]) * inv),
+                                                pack_bf16x2(__uint_as_float(ov[8 * u + 6]) * inv, __uint_as_float(ov[8 * u + 7]) * inv));
                     }
                 }
                 if (row_in)
@@ -333,7 +430,7 @@ __global__ void __launch_bounds__(192, 2)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -341,22 +438,24 @@ __global__ void __launch_bounds__(192, 2)
 
 using namespace fm;
 
-fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const FwdArgs &a, int d, cudaStream_t stream)
+template <int D, bool PRECISE>
+static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const FwdArgs &a, cudaStream_t stream)
 {
-    const dim3 grid(a.L.n_q, a.H, a.B);
-    if (d == 128) {
-        constexpr int smem = FwdSmem<128>::kBytes;
-        if (cudaFuncSetAttribute(fm_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return FM_ERR_CUDA;
-        ProfScope ps(kKFwd, stream);
-        fm_fwd_kernel<128><<<grid, 192, smem, stream>>>(tq, tk, tv, a);
-    } else {
-        constexpr int smem = FwdSmem<64>::kBytes;
-        if (cudaFuncSetAttribute(fm_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return FM_ERR_CUDA;
-        ProfScope ps(kKFwd, stream);
-        fm_fwd_kernel<64><<<grid, 192, smem, stream>>>(tq, tk, tv, a);
-    }
+    constexpr int smem = FwdSmem<D>::kBytes;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    if (cudaFuncSetAttribute(fm_fwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return FM_ERR_CUDA;
+    ProfScope ps(kKFwd, stream);
+    fm_fwd_kernel<D, PRECISE><<<dim3((a.L.n_q + 1) / 2, a.H, a.B), 320, smem, stream>>>(tq, tk, tv, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const FwdArgs &a, int d, bool precise, cudaStream_t stream)
+{
+    if (d == 128)
+        return precise ? launch_fwd<128, true>(tq, tk, tv, a, stream) : launch_fwd<128, false>(tq, tk, tv, a, stream);
+    return precise ? launch_fwd<64, true>(tq, tk, tv, a, stream) : launch_fwd<64, false>(tq, tk, tv, a, stream);
 }

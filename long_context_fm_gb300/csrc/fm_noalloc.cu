@@ -50,7 +50,7 @@ fm_status scratch_address(void **out)
 extern "C" fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                          int o_dtype, const float *lse, const void *dO, fm_bounds m,
                                          const void *plan, int B, int H, int N, int d, float scale,
-                                         void *dq, void *dk, void *dv, int grad_dtype,
+                                         void *dq, void *dk, void *dv, int grad_dtype, int flags,
                                          int32_t *dev_status, fm_stream_t stream)
 {
     const size_t need = fm_bwd_workspace_bytes(B, H, N, d);
@@ -63,5 +63,5 @@ extern "C" fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const voi
     // before the main kernel reads them, so the previous call's contents of
     // the array never leak into this one.
     return fm_attn_bwd(q, k, v, o, o_dtype, lse, dO, m, plan, B, H, N, d, scale, dq, dk, dv,
-                       grad_dtype, ws, (size_t)FM_NOALLOC_SCRATCH_BYTES, dev_status, stream);
+                       grad_dtype, flags, ws, (size_t)FM_NOALLOC_SCRATCH_BYTES, dev_status, stream);
 }

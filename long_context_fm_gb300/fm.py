@@ -22,6 +22,7 @@ FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_UNREPRESENTABLE = 0, 1, 2,
 FM_ERR_BAD_BOUNDS, FM_ERR_PLAN_MISMATCH, FM_ERR_WORKSPACE, FM_ERR_CUDA, FM_ERR_TIMEOUT = 4, 5, 6, 7, 8
 FM_TILE_SKIP, FM_TILE_FULL, FM_TILE_PARTIAL = 0, 1, 2
 FM_DT_BF16, FM_DT_F32 = 0, 1
+FM_FLAG_PRECISE = 1
 KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post"]
 
 EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_plan_bytes",
@@ -58,13 +59,13 @@ _lib.fm_plan_bytes.argtypes = [_I, _I, _I, _I, _I]
 _lib.fm_tile_classify.argtypes = [Bounds, _I, _I, _P, _SZ, _P, _P, _P]
 _lib.fm_fwd_workspace_bytes.restype = _SZ
 _lib.fm_fwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
-_lib.fm_attn_fwd.argtypes = [_P, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _P, _P]
+_lib.fm_attn_fwd.argtypes = [_P, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _I, _P, _P]
 _lib.fm_bwd_workspace_bytes.restype = _SZ
 _lib.fm_bwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
 _lib.fm_attn_bwd.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _P, _P,
-                             _I, _P, _SZ, _P, _P]
+                             _I, _I, _P, _SZ, _P, _P]
 _lib.fm_attn_bwd_noalloc.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P,
-                                     _P, _P, _I, _P, _P]
+                                     _P, _P, _I, _I, _P, _P]
 _lib.fm_profile_begin.argtypes = []
 _lib.fm_profile_end.restype = _I
 _lib.fm_profile_end.argtypes = [_P, _I]
@@ -156,7 +157,8 @@ def fm_fwd_workspace_bytes(B, H, N, d) -> int:
     return int(_lib.fm_fwd_workspace_bytes(B, H, N, d))
 
 
-def fm_attn_fwd(q, k, v, bounds: Bounds, plan, scale, o, lse, dev_status, ws=None, stream=None):
+def fm_attn_fwd(q, k, v, bounds: Bounds, plan, scale, o, lse, dev_status, ws=None, stream=None,
+                flags=0):
     for n, t in (("q", q), ("k", k), ("v", v)):
         _dev(t, torch.bfloat16, n)
     B, H, N, d = q.shape
@@ -168,7 +170,7 @@ def fm_attn_fwd(q, k, v, bounds: Bounds, plan, scale, o, lse, dev_status, ws=Non
     _dev(dev_status, torch.int32, "dev_status")
     code = _lib.fm_attn_fwd(_ptr(q), _ptr(k), _ptr(v), bounds, _ptr(plan), B, H, N, d, float(scale),
                             _ptr(o), _dt(o), _ptr(lse), _ptr(ws), 0 if ws is None else ws.numel(),
-                            _ptr(dev_status), _stream(stream))
+                            int(flags), _ptr(dev_status), _stream(stream))
     _check(code, "fm_attn_fwd")
 
 
@@ -177,7 +179,7 @@ def fm_bwd_workspace_bytes(B, H, N, d) -> int:
 
 
 def fm_attn_bwd(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk, dv, ws, dev_status,
-                stream=None):
+                stream=None, flags=0):
     for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
         _dev(t, torch.bfloat16, n)
     B, H, N, d = q.shape
@@ -191,12 +193,12 @@ def fm_attn_bwd(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk, dv, ws
     _dev(ws, torch.uint8, "ws")
     code = _lib.fm_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(lse), _ptr(dO), bounds,
                             _ptr(plan), B, H, N, d, float(scale), _ptr(dq), _ptr(dk), _ptr(dv),
-                            _dt(dq), _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
+                            _dt(dq), int(flags), _ptr(ws), ws.numel(), _ptr(dev_status), _stream(stream))
     _check(code, "fm_attn_bwd")
 
 
 def fm_attn_bwd_noalloc(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk, dv, dev_status,
-                        stream=None):
+                        stream=None, flags=0):
     """fm_attn_bwd without a caller workspace: for callers that cannot
     allocate device memory; the library's fixed built-in array is used
     instead (see fm.h for the size limit and the rules on overlapping calls)."""
@@ -212,7 +214,7 @@ def fm_attn_bwd_noalloc(q, k, v, o, lse, dO, bounds: Bounds, plan, scale, dq, dk
     _dev(lse, torch.float32, "lse")
     code = _lib.fm_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(lse), _ptr(dO),
                                     bounds, _ptr(plan), B, H, N, d, float(scale), _ptr(dq), _ptr(dk),
-                                    _ptr(dv), _dt(dq), _ptr(dev_status), _stream(stream))
+                                    _ptr(dv), _dt(dq), int(flags), _ptr(dev_status), _stream(stream))
     _check(code, "fm_attn_bwd_noalloc")
 
 
@@ -262,22 +264,23 @@ class MaskedAttention:
         fm_tile_classify(self.bounds, plan, self.status, bq, bk, labels=out, stream=self.stream)
         return out
 
-    def forward(self, q, k, v, scale=None, o_dtype=torch.bfloat16):
+    def forward(self, q, k, v, scale=None, o_dtype=torch.bfloat16, flags=0):
         B, H, N, d = q.shape
         scale = 1.0 / d ** 0.5 if scale is None else scale
         o = torch.empty(q.shape, dtype=o_dtype, device=q.device)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-        fm_attn_fwd(q, k, v, self.bounds, self.plan, scale, o, lse, self.status, stream=self.stream)
+        fm_attn_fwd(q, k, v, self.bounds, self.plan, scale, o, lse, self.status, stream=self.stream,
+                    flags=flags)
         return o, lse
 
-    def backward(self, q, k, v, o, lse, dO, scale=None, grad_dtype=torch.float32, ws=None):
+    def backward(self, q, k, v, o, lse, dO, scale=None, grad_dtype=torch.float32, ws=None, flags=0):
         B, H, N, d = q.shape
         scale = 1.0 / d ** 0.5 if scale is None else scale
         if ws is None:
             ws = torch.empty(fm_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
         dq, dk, dv = (torch.empty(q.shape, dtype=grad_dtype, device=q.device) for _ in range(3))
         fm_attn_bwd(q, k, v, o, lse, dO, self.bounds, self.plan, scale, dq, dk, dv, ws, self.status,
-                    stream=self.stream)
+                    stream=self.stream, flags=flags)
         return dq, dk, dv
 
     def check_status(self):

@@ -57,5 +57,5 @@ def test_noalloc_refuses_sizes_beyond_the_builtin_array(fm):
     assert fm.fm_bwd_workspace_bytes(B, H, N, d) > fm.NOALLOC_SCRATCH_BYTES
     bounds = fm.Bounds(None, None, None, None, B, 1, N)
     code = fm._lib.fm_attn_bwd_noalloc(None, None, None, None, 0, None, None, bounds, None, B, H, N,
-                                       d, ctypes.c_float(0.1), None, None, None, 1, None, None)
+                                       d, ctypes.c_float(0.1), None, None, None, 1, 0, None, None)
     assert code == fm.FM_ERR_WORKSPACE
