@@ -284,7 +284,7 @@ fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o
     float *dq_acc = reinterpret_cast<float *>(ws);
     if (!make_tmap_bf16(&tq, q, B * H, N, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
         !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, N, d, 64) ||
-        !make_tmap_f32_rows(&tdq, dq_acc, B * H, N, d, 64))
+        !make_tmap_f32_rows(&tdq, dq_acc, B * H, N, d, 32))
         return FM_ERR_CUDA;
     float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * N * d * 4));
     const int64_t rows = (int64_t)B * H * N;

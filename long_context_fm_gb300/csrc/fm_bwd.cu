@@ -12,12 +12,13 @@
 // two 64-row halves.
 //   warp 0      TMA producer (K and V once; Q, dO halves double-buffered;
 //               lse and D staged into shared memory by the whole warp)
-//   warp 1      TMEM allocation; one thread issues the tcgen05 MMAs
+//   warp 1      TMEM allocation; one thread issues the score MMAs (S^T, dP^T)
 //   warps 2-9   two warpgroups, one thread per KV row j each: P^T and dS^T
 //               for columns [0, 32) and [32, 64) of the half
 //   warps 10-13 one thread per head-dim index: drain dQ^T from TMEM into the
 //               fp32 dQ accumulator (standard mode: shared-memory tile plus a
 //               bulk tensor reduce-add; precise mode: red.global.add)
+//   warp 14     one thread issues the gradient MMAs (dV, dK, dQ^T)
 // TMEM (512 columns): dK [0, d), dV [128, 128 + d), S^T [256, 320),
 // dP^T [320, 384), dQ^T [384, 448).  Per half (M = 128 KV rows):
 //   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
@@ -100,32 +101,35 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, v
 // ---------------------------------------------------------------- main kernel
 template <int D, bool PRECISE>
 struct BwdSmem {
+    // Q/dO stages: three in standard mode; precise mode needs the room for
+    // the low operand terms and keeps two.
+    static constexpr int kStages = PRECISE ? 2 : 3;
     static constexpr int kKBox = 128 * 128;     // 64 columns x 128 rows
     static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
     static constexpr int kKTile = 128 * D * 2;
     static constexpr int kQTile = 64 * D * 2;
     static constexpr int kOp = 128 * 128;       // one 128 x 64 bf16 operand tile
     static constexpr int kK = 0, kV = kKTile;
-    static constexpr int kQ = 2 * kKTile;                   // [2] stages
-    static constexpr int kdO = kQ + 2 * kQTile;             // [2] stages
-    static constexpr int kP = kdO + 2 * kQTile;             // P^T  (high part)
+    static constexpr int kQ = 2 * kKTile;                   // [kStages]
+    static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
+    static constexpr int kP = kdO + kStages * kQTile;       // P^T  (high part)
     static constexpr int kdS = kP + kOp;                    // dS^T (high part)
     static constexpr int kPlo = kdS + kOp;                  // precise: P^T low part
     static constexpr int kdSlo = kPlo + kOp;                // precise: dS^T low part
-    static constexpr int kDQ = PRECISE ? kdSlo + kOp : kPlo; // standard: fp32 dQ tile [64][D]
-    static constexpr int kList = PRECISE ? kDQ : kDQ + 64 * D * 4;
+    static constexpr int kDQ = PRECISE ? kdSlo + kOp : kPlo; // standard: fp32 dQ tile [32][D]
+    static constexpr int kList = PRECISE ? kDQ : kDQ + 32 * D * 4;
     static constexpr int kListCap = 2048;                   // Q tiles staged from the plan
-    static constexpr int kStat = kList + kListCap * 4;      // lse2 [2][64], D [2][64]
-    static constexpr int kBar = kStat + 4 * 64 * 4;
-    static constexpr int kNumBar = 16;
+    static constexpr int kStat = kList + kListCap * 4;      // lse2 [kStages][64], D [kStages][64]
+    static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
+    static constexpr int kNumBar = 20;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
 };
 
 enum {
-    BB_KV = 0, BB_QF0, BB_QF1, BB_QE0, BB_QE1, BB_SF, BB_SE, BB_PF, BB_DSE, BB_DQF, BB_DQE, BB_ACC,
-    BB_DRAIN, BB_STF, BB_STE
+    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF, BB_SE, BB_PF, BB_DSE, BB_DQF0,
+    BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_STF, BB_STE
 };
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
@@ -151,7 +155,7 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D, bool PRECISE>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(480, 1)
     fm_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const BwdArgs a)
@@ -166,8 +170,9 @@ __global__ void __launch_bounds__(448, 1)
     uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS, *sPlo = smem + S::kPlo, *sdSlo = smem + S::kdSlo;
     float *sDQ = reinterpret_cast<float *>(smem + S::kDQ);
     int32_t *sList = reinterpret_cast<int32_t *>(smem + S::kList);
-    float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [2][64]
-    float *sD = sLse + 128;                                          // [2][64]
+    constexpr int NST = S::kStages;
+    float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [NST][64]
+    float *sD = sLse + NST * 64;                                     // [NST][64]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
@@ -191,18 +196,21 @@ __global__ void __launch_bounds__(448, 1)
         *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)sidx * L.n_k + kt] : 0;
         *abort = 0;
         mbar_init(&bars[BB_KV], 1);
-        mbar_init(&bars[BB_QF0], 33);
-        mbar_init(&bars[BB_QF1], 33);
-        mbar_init(&bars[BB_QE0], 1);
-        mbar_init(&bars[BB_QE1], 1);
+        for (int s2 = 0; s2 < NST; ++s2) {
+            mbar_init(&bars[BB_QF0 + s2], 33);
+            mbar_init(&bars[BB_QE0 + s2], 2);     // scores and gradients issuers
+        }
         mbar_init(&bars[BB_SF], 1);
         mbar_init(&bars[BB_SE], 256);
         mbar_init(&bars[BB_PF], 256);
         mbar_init(&bars[BB_DSE], 1);
-        mbar_init(&bars[BB_DQF], 1);
-        mbar_init(&bars[BB_DQE], 128);
+        mbar_init(&bars[BB_DQF0], 1);
+        mbar_init(&bars[BB_DQF1], 1);
+        mbar_init(&bars[BB_DQE0], 128);
+        mbar_init(&bars[BB_DQE1], 128);
         mbar_init(&bars[BB_ACC], 1);
-        mbar_init(&bars[BB_DRAIN], 1);
+        mbar_init(&bars[BB_DRAIN0], 1);
+        mbar_init(&bars[BB_DRAIN1], 1);
         mbar_init(&bars[BB_STF], 128);
         mbar_init(&bars[BB_STE], 1);
         fence_barrier_init();
@@ -215,6 +223,7 @@ __global__ void __launch_bounds__(448, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // TMEM: dK, dV, S^T, dP^T, and dQ^T double-buffered (half it uses buffer it & 1).
     const uint32_t tdK = tmem, tdV = tmem + 128, tS = tmem + 256, tdP = tmem + 320, tdQ = tmem + 384;
     const int cnt = *cnt_sh;
     const int32_t *glist =
@@ -245,7 +254,7 @@ __global__ void __launch_bounds__(448, 1)
             int it = 0;
             for (; it < n_it; ++it) {
                 const int q0 = q0_of(it);
-                const int st = it & 1;
+                const int st = it % NST;
                 // lse and D of the half's rows, loaded before the stage wait so
                 // the global latency overlaps it; rows beyond N get P = 0.
                 float lv[2], dv[2];
@@ -259,7 +268,7 @@ __global__ void __launch_bounds__(448, 1)
                         dv[rr] = a.Dvec[(int64_t)bh * N + qi];
                     }
                 }
-                if (it >= 2 && !warp_wait(&bars[BB_QE0 + st], ((it >> 1) - 1) & 1, abort, a.status)) break;
+                if (it >= NST && !warp_wait(&bars[BB_QE0 + st], ((it / NST) - 1) & 1, abort, a.status)) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
 #pragma unroll
@@ -279,85 +288,92 @@ __global__ void __launch_bounds__(448, 1)
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
                 if (n_it > 0) mbar_wait_drain(&bars[BB_KV], 0, a.status);
-                for (int k2 = (it > 2 ? it - 2 : 0); k2 < it; ++k2)
-                    mbar_wait_drain(&bars[BB_QF0 + (k2 & 1)], (k2 >> 1) & 1, a.status);
+                for (int k2 = (it > NST ? it - NST : 0); k2 < it; ++k2)
+                    mbar_wait_drain(&bars[BB_QF0 + (k2 % NST)], (k2 / NST) & 1, a.status);
             }
-        } else if (warp == 1) {
-            // ------------------------------------------------ MMA issuer
-            // Issue order per half `it`: S/dP of it+1 as soon as the S buffer
-            // is drained, then dV, dK, dQ of it; the tensor core computes the
-            // next scores while the P/dS warps work on the current ones.
+        } else if (warp == 1 || warp == 14) {
+            // ------------------------------------------------ MMA issuers
+            // Two issuing threads: warp 1 issues the scores S^T, dP^T of each
+            // half as soon as its Q/dO have landed and the S buffer is drained;
+            // warp 14 issues the gradient products dV, dK, dQ^T of each half as
+            // soon as its P/dS are written.  Each blocks on the tensor-core
+            // queue independently, so the next scores are never held back
+            // behind the current gradients (or the reverse).  A Q/dO stage is
+            // released by one commit from each thread.
+            const bool scores = (warp == 1);
             if (lane == 0 && n_it > 0) {
                 constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
                 constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
                 constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
                 constexpr int NPART = PRECISE ? 2 : 1;
-                const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-                const uint32_t aP[2] = {smem_u32(sP), smem_u32(sPlo)};
-                const uint32_t adS[2] = {smem_u32(sdS), smem_u32(sdSlo)};
-                auto issue_scores = [&](int it) {
-                    const int st = it & 1;
-                    const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
-                        const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                        mma_ss(tS, sdesc_sw128(aK + ok_, 16, 1024), sdesc_sw128(aQ + oq, 16, 1024), idS, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
-                        const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                        mma_ss(tdP, sdesc_sw128(aV + ok_, 16, 1024), sdesc_sw128(adO + oq, 16, 1024), idS, kk > 0);
-                    }
-                    tc_commit(&bars[BB_SF]);
-                };
-                bool ok = mbar_wait(&bars[BB_KV], 0, abort, a.status) && mbar_wait(&bars[BB_QF0], 0, abort, a.status);
-                if (ok) {
-                    tc_fence_after();
-                    issue_scores(0);
-                }
-                int it = 0;
-                for (; ok && it < n_it; ++it) {
-                    const int st = it & 1;
-                    if (it + 1 < n_it) {
-                        if (!mbar_wait(&bars[BB_QF0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, abort, a.status) ||
-                            !mbar_wait(&bars[BB_SE], it & 1, abort, a.status)) { ok = false; break; }
+                const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024);      // K, K-major
+                const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);      // V, K-major
+                const uint64_t dKm = sdesc_sw128(smem_u32(sK), S::kKBox, 1024); // K, MN-major
+                const uint64_t dP[2] = {sdesc_sw128(smem_u32(sP), 16, 1024), sdesc_sw128(smem_u32(sPlo), 16, 1024)};
+                const uint64_t dSk[2] = {sdesc_sw128(smem_u32(sdS), 16, 1024), sdesc_sw128(smem_u32(sdSlo), 16, 1024)};
+                const uint64_t dSm[2] = {sdesc_sw128(smem_u32(sdS), S::kKBox, 1024),
+                                         sdesc_sw128(smem_u32(sdSlo), S::kKBox, 1024)};
+                bool ok = mbar_wait(&bars[BB_KV], 0, abort, a.status);
+                for (int it = 0; ok && it < n_it; ++it) {
+                    const int st = it % NST;
+                    const uint64_t dQk = sdesc_sw128(smem_u32(sQ + st * S::kQTile), 16, 1024);
+                    const uint64_t dOk = sdesc_sw128(smem_u32(sdO + st * S::kQTile), 16, 1024);
+                    if (scores) {
+                        if (!mbar_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status) ||
+                            (it > 0 && !mbar_wait(&bars[BB_SE], (it - 1) & 1, abort, a.status))) { ok = false; break; }
                         tc_fence_after();
-                        issue_scores(it + 1);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                            mma_ss(tS, sdesc_add(dKk, ok_), sdesc_add(dQk, oq), idS, kk > 0);
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                            mma_ss(tdP, sdesc_add(dVk, ok_), sdesc_add(dOk, oq), idS, kk > 0);
+                        }
+                        tc_commit(&bars[BB_SF]);
+                        tc_commit(&bars[BB_QE0 + st]);
+                    } else {
+                        const int qb = it & 1;         // dQ^T buffer
+                        if (!mbar_wait(&bars[BB_PF], it & 1, abort, a.status) ||
+                            (it >= 2 && !mbar_wait(&bars[BB_DQE0 + qb], ((it >> 1) - 1) & 1, abort, a.status))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
+                        const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
+#pragma unroll
+                        for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                       (it > 0 || part > 0 || kk > 0));
+#pragma unroll
+                        for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tdK, sdesc_add(dSk[part], kk * 32), sdesc_add(dQm, kk * 2048), idKV,
+                                       (it > 0 || part > 0 || kk > 0));
+#pragma unroll
+                        for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_ss(tdQ + qb * 64, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], kk * 2048), idQ,
+                                       (part > 0 || kk > 0));
+                        tc_commit(&bars[BB_DQF0 + qb]);
+                        tc_commit(&bars[BB_DSE]);
+                        tc_commit(&bars[BB_QE0 + st]);
                     }
-                    if (!mbar_wait(&bars[BB_PF], it & 1, abort, a.status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t aQ = smem_u32(sQ + st * S::kQTile), adO = smem_u32(sdO + st * S::kQTile);
-#pragma unroll
-                    for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tdV, sdesc_sw128(aP[part] + kk * 32, 16, 1024),
-                                   sdesc_sw128(adO + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || part > 0 || kk > 0));
-#pragma unroll
-                    for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tdK, sdesc_sw128(adS[part] + kk * 32, 16, 1024),
-                                   sdesc_sw128(aQ + kk * 2048, S::kQBox, 1024), idKV, (it > 0 || part > 0 || kk > 0));
-                    if (it > 0 && !mbar_wait(&bars[BB_DQE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ss(tdQ, sdesc_sw128(aK + kk * 2048, S::kKBox, 1024),
-                                   sdesc_sw128(adS[part] + kk * 2048, S::kKBox, 1024), idQ, (part > 0 || kk > 0));
-                    tc_commit(&bars[BB_DQF]);
-                    tc_commit(&bars[BB_DSE]);
-                    tc_commit(&bars[BB_QE0 + st]);
                 }
-                if (ok) tc_commit(&bars[BB_ACC]);
+                if (ok && !scores) tc_commit(&bars[BB_ACC]);
             }
             if (lane == 0) {
-                tc_commit(&bars[BB_DRAIN]);
-                mbar_wait_drain(&bars[BB_DRAIN], 0, a.status);
+                tc_commit(&bars[BB_DRAIN0 + (scores ? 0 : 1)]);
+                mbar_wait_drain(&bars[BB_DRAIN0 + (scores ? 0 : 1)], 0, a.status);
             }
         } else if (warp < 10) {
             // ------------------------------------------------ P^T / dS^T
@@ -380,9 +396,9 @@ __global__ void __launch_bounds__(448, 1)
             for (int it = 0; it < n_it; ++it) {
                 const int q0 = q0_of(it);
                 const bool pred = ((entry(it >> 1) >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
-                const int st = it & 1;
+                const int st = it % NST;
                 if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
-                    !warp_wait(&bars[BB_QF0 + st], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                    !warp_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status)) { ok = false; break; }
                 tc_fence_after();
                 const float *l2 = sLse + st * 64 + c0;
                 const float *dd = sD + st * 64 + c0;
@@ -473,26 +489,29 @@ __global__ void __launch_bounds__(448, 1)
                     }
                 }
             }
-        } else {
+        } else if (warp < 14) {
             // ------------------------------------------------ dQ drain
             // Thread = head-dim index (TMEM lane of dQ^T).  Standard mode:
-            // the 64 x d tile goes through shared memory and one bulk
-            // reduce-add per half; precise mode: coalesced red.global.add.
+            // the 64 x d tile goes through a 32-row shared-memory tile and two
+            // bulk tensor reduce-adds per half; precise mode: coalesced
+            // red.global.add.
             const int quarter = warp & 3;
             const int dd = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const bool leader = (warp == 10 && lane == 0);
+            int sub = 0;   // staging-tile uses so far
             for (int it = 0; it < n_it; ++it) {
                 const int q0 = q0_of(it);
-                if (!warp_wait(&bars[BB_DQF], it & 1, abort, a.status)) break;
+                const int qb = it & 1;
+                if (!warp_wait(&bars[BB_DQF0 + qb], (it >> 1) & 1, abort, a.status)) break;
                 tc_fence_after();
                 uint32_t v[2][32];
-                tmem_ld32(tdQ + lane_off, v[0]);
-                tmem_ld32(tdQ + lane_off + 32, v[1]);
+                tmem_ld32(tdQ + qb * 64 + lane_off, v[0]);
+                tmem_ld32(tdQ + qb * 64 + lane_off + 32, v[1]);
                 tmem_ld_wait();
                 tmem_reg_fence(v[0]); tmem_reg_fence(v[1]);
                 tc_fence_before();
-                mbar_arrive(&bars[BB_DQE]);
+                mbar_arrive(&bars[BB_DQE0 + qb]);
                 if (PRECISE) {
                     if (dd < D) {
                         float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
@@ -502,22 +521,28 @@ __global__ void __launch_bounds__(448, 1)
                             if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
                     }
                 } else {
-                    if (it > 0 && !warp_wait(&bars[BB_STE], (it - 1) & 1, abort, a.status)) break;
-                    if (dd < D) {
+                    bool okq = true;
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) sDQ[c * D + dd] = __uint_as_float(v[c >> 5][c & 31]);
-                    }
-                    fence_proxy_async_smem();
-                    mbar_arrive(&bars[BB_STF]);
-                    if (leader) {
-                        // Rows beyond N are clipped by the tensor map.
-                        if (mbar_wait(&bars[BB_STF], it & 1, abort, a.status)) {
-                            tma_reduce_add_3d(&tdq, sDQ, 0, q0, bh);
-                            bulk_commit();
-                            bulk_wait_read0();
+                    for (int hh = 0; hh < 2; ++hh, ++sub) {
+                        if (q0 + hh * 32 >= N) break;            // rows beyond N: nothing to add
+                        if (sub > 0 && !warp_wait(&bars[BB_STE], (sub - 1) & 1, abort, a.status)) { okq = false; break; }
+                        if (dd < D) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) sDQ[c * D + dd] = __uint_as_float(v[hh][c]);
                         }
-                        mbar_arrive(&bars[BB_STE]);
+                        fence_proxy_async_smem();
+                        mbar_arrive(&bars[BB_STF]);
+                        if (leader) {
+                            // Rows beyond N are clipped by the tensor map.
+                            if (mbar_wait(&bars[BB_STF], sub & 1, abort, a.status)) {
+                                tma_reduce_add_3d(&tdq, sDQ, 0, q0 + hh * 32, bh);
+                                bulk_commit();
+                                bulk_wait_read0();
+                            }
+                            mbar_arrive(&bars[BB_STE]);
+                        }
                     }
+                    if (!okq) break;
                 }
             }
             if (!PRECISE && leader) bulk_wait0();   // reductions complete before exit
@@ -561,7 +586,7 @@ static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
         cudaSuccess)
         return FM_ERR_CUDA;
     ProfScope ps(kKBwd, stream);
-    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 448, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 480, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 

@@ -14,15 +14,17 @@
 // never loaded.  Roles:
 //   warp 0      TMA producer: Q0, Q1 once; K and V through a two-stage ring;
 //               the column bounds of partial tiles into shared memory
-//   warp 1      allocates TMEM; one thread issues the tcgen05 MMAs
+//   warp 1      allocates TMEM; one thread issues the tcgen05 MMAs of Q0
 //   warps 2-5   softmax of Q0, one thread per row = TMEM lane
 //   warps 6-9   softmax of Q1
+//   warp 10     one thread issues the tcgen05 MMAs of Q1
 // TMEM (512 columns): S0, S1 = Qi K^T at [0, 128) and [128, 256), each
 // overwritten in place by P as packed bf16 (the A operand of Oi += P V; in
 // precise mode a second term P_lo = bf16(P - bf16(P)) follows in the upper
 // 64 columns and Oi += P_hi V + P_lo V); O0, O1 accumulate at [256, 384) and
-// [384, 512).  The two softmax warpgroups ping-pong: while one works on its
-// scores the tensor core runs the other tile's products.
+// [384, 512).  The two (Q tile, softmax, issuer) streams run independently:
+// while one softmax works on its scores the tensor core runs the other
+// tile's products.
 // Online softmax in the base-2 domain with a lazy rescale: O and l are
 // rescaled only when the row max grows by more than 2^8, which keeps every
 // P <= 256 and leaves the final O / l unchanged.
@@ -56,7 +58,7 @@ struct FwdSmem {
 
 enum {
     FB_Q = 0, FB_KF0, FB_KF1, FB_KE0, FB_KE1, FB_VF0, FB_VF1, FB_VE0, FB_VE1, FB_BF0, FB_BF1,
-    FB_S0, FB_S1, FB_P0, FB_P1, FB_O0, FB_O1, FB_DRAIN
+    FB_S0, FB_S1, FB_P0, FB_P1, FB_O0, FB_O1, FB_DRAIN0, FB_DRAIN1
 };
 
 // Walks the union of two ascending lists of KV tiles (entries tile | label << 28).
@@ -82,7 +84,7 @@ struct TileMerge {
 };
 
 template <int D, bool PRECISE>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fm_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a)
 {
@@ -123,15 +125,16 @@ __global__ void __launch_bounds__(320, 1)
         mbar_init(&bars[FB_Q], 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars[FB_KF0 + s], 1);
-            mbar_init(&bars[FB_KE0 + s], 1);
+            mbar_init(&bars[FB_KE0 + s], 2);    // one arrival per stream
             mbar_init(&bars[FB_VF0 + s], 1);
-            mbar_init(&bars[FB_VE0 + s], 1);
+            mbar_init(&bars[FB_VE0 + s], 2);
             mbar_init(&bars[FB_BF0 + s], 32);
             mbar_init(&bars[FB_S0 + s], 1);
             mbar_init(&bars[FB_P0 + s], 128);
             mbar_init(&bars[FB_O0 + s], 1);
         }
-        mbar_init(&bars[FB_DRAIN], 1);
+        mbar_init(&bars[FB_DRAIN0], 1);
+        mbar_init(&bars[FB_DRAIN1], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -227,63 +230,69 @@ __global__ void __launch_bounds__(320, 1)
                     mbar_wait_drain(&bars[FB_VF0 + (k2 & 1)], (k2 >> 1) & 1, a.status);
                 }
             }
-        } else if (warp == 1) {
-            // ------------------------------------------------ MMA issuer
+        } else if (warp == 1 || warp == 10) {
+            // ------------------------------------------------ MMA issuers
+            // One issuing thread per Q tile (warp 1 for Q0, warp 10 for Q1):
+            // each alternates S_q = Q_q K^T and O_q += P_q V over its own
+            // tiles, so one stream blocking on the tensor-core queue or on its
+            // softmax never holds back the other.  Both threads walk every
+            // tile of the union: a tile's K (V) stage is released by one
+            // arrival per stream, a commit after its S (PV) if the stream needs
+            // the tile, a plain arrive after seeing the tile land if not.
             if (lane == 0 && any) {
+                const int q = (warp == 1) ? 0 : 1;
                 constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
                 constexpr uint32_t idO = idesc_bf16(128, D, false, true);
                 constexpr int NPART = PRECISE ? 2 : 1;
-                const uint32_t aQ[2] = {smem_u32(smem + S::kQ0), smem_u32(smem + S::kQ1)};
-                int c[2] = {0, 0};
+                const uint64_t dQ = sdesc_sw128(smem_u32(smem + (q ? S::kQ1 : S::kQ0)), 16, 1024);
+                const uint32_t tSq = tmem + q * 128, tOq = tmem + 256 + q * 128;
                 bool ok = mbar_wait(&bars[FB_Q], 0, abort, a.status);
-                int t = 0, kt, lab[2];
+                int c = 0, t = 0, kt, lab[2];
                 for (; ok && walk.next(kt, lab[0], lab[1]); ++t) {
                     const int st = t & 1;
                     const uint32_t ph = (t >> 1) & 1;
-                    const uint32_t aK = smem_u32(smem + S::kK + st * S::kTile);
-                    const uint32_t aV = smem_u32(smem + S::kV + st * S::kTile);
+                    const bool mine = lab[q] >= 0;
                     if (!mbar_wait(&bars[FB_KF0 + st], ph, abort, a.status)) { ok = false; break; }
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        if (lab[q] < 0) continue;
-                        // S_q aliases P_q of the previous tile: wait for that PV.
-                        if (c[q] > 0 && !mbar_wait(&bars[FB_O0 + q], (c[q] - 1) & 1, abort, a.status)) { ok = false; break; }
+                    if (mine) {
+                        // S_q aliases P_q of this stream's previous tile: wait for that PV.
+                        if (c > 0 && !mbar_wait(&bars[FB_O0 + q], (c - 1) & 1, abort, a.status)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dK = sdesc_sw128(smem_u32(smem + S::kK + st * S::kTile), 16, 1024);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * S::kBox + (kk & 3) * 32;
-                            mma_ss(tmem + q * 128, sdesc_sw128(aQ[q] + off, 16, 1024),
-                                   sdesc_sw128(aK + off, 16, 1024), idS, kk > 0);
+                            mma_ss(tSq, sdesc_add(dQ, off), sdesc_add(dK, off), idS, kk > 0);
                         }
                         tc_commit(&bars[FB_S0 + q]);
+                        tc_commit(&bars[FB_KE0 + st]);
+                    } else {
+                        mbar_arrive(&bars[FB_KE0 + st]);
                     }
-                    if (!ok) break;
-                    tc_commit(&bars[FB_KE0 + st]);
                     if (!mbar_wait(&bars[FB_VF0 + st], ph, abort, a.status)) { ok = false; break; }
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        if (lab[q] < 0) continue;
-                        if (!mbar_wait(&bars[FB_P0 + q], c[q] & 1, abort, a.status)) { ok = false; break; }
+                    if (mine) {
+                        if (!mbar_wait(&bars[FB_P0 + q], c & 1, abort, a.status)) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dV = sdesc_sw128(smem_u32(smem + S::kV + st * S::kTile), S::kBox, 1024);
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)   // P_hi V (+ P_lo V)
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)
-                                mma_ts(tmem + 256 + q * 128, tmem + q * 128 + part * 64 + kk * 8,
-                                       sdesc_sw128(aV + kk * 2048, S::kBox, 1024), idO, (c[q] > 0 || part > 0 || kk > 0));
+                                mma_ts(tOq, tSq + part * 64 + kk * 8, sdesc_add(dV, kk * 2048), idO,
+                                       (c > 0 || part > 0 || kk > 0));
                         tc_commit(&bars[FB_O0 + q]);
-                        ++c[q];
+                        tc_commit(&bars[FB_VE0 + st]);
+                        ++c;
+                    } else {
+                        mbar_arrive(&bars[FB_VE0 + st]);
                     }
-                    if (!ok) break;
-                    tc_commit(&bars[FB_VE0 + st]);
                 }
             }
             if (lane == 0) {
                 // Every MMA of this CTA completes before TMEM is released.
-                tc_commit(&bars[FB_DRAIN]);
-                mbar_wait_drain(&bars[FB_DRAIN], 0, a.status);
+                tc_commit(&bars[FB_DRAIN0 + (warp == 1 ? 0 : 1)]);
+                mbar_wait_drain(&bars[FB_DRAIN0 + (warp == 1 ? 0 : 1)], 0, a.status);
             }
-        } else {
+        } else if (warp < 10) {
             // ------------------------------------------------ softmax (Q0: warps 2-5, Q1: warps 6-9)
             const int q = (warp < 6) ? 0 : 1;
             const int quarter = warp & 3;
@@ -448,7 +457,7 @@ static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
         cudaSuccess)
         return FM_ERR_CUDA;
     ProfScope ps(kKFwd, stream);
-    fm_fwd_kernel<D, PRECISE><<<dim3((a.L.n_q + 1) / 2, a.H, a.B), 320, smem, stream>>>(tq, tk, tv, a);
+    fm_fwd_kernel<D, PRECISE><<<dim3((a.L.n_q + 1) / 2, a.H, a.B), 352, smem, stream>>>(tq, tk, tv, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 

@@ -67,6 +67,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test (never suspends the thread): for issuers that poll
+// several barriers and must move on at once when one is not ready.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Same test, but a thread whose phase is not complete yet may be suspended
+// (up to `hint_ns`) until it completes, instead of spinning on issue slots
+// that the sub-partition's working warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendHintNs = 20000;
+
 // Waits for the phase with the given parity to complete.  Returns false
 // (after raising *abort and recording FM_ERR_TIMEOUT) when `limit` cycles pass
 // first, or when another thread of the CTA has already aborted.
@@ -76,7 +109,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
         if (*abort) return false;
         if (clock64() - t0 > limit) {
             set_status(status, FM_ERR_TIMEOUT);
@@ -94,7 +127,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
         if (clock64() - t0 > limit) {
             set_status(status, FM_ERR_TIMEOUT);
             return false;
@@ -199,6 +232,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Descriptor of the same operand `byte_off` bytes further on (the start
+// address field never carries out of its 14 bits inside shared memory).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t base, uint32_t byte_off)
+{
+    return base + (uint64_t)(byte_off >> 4);
 }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulate.

@@ -81,6 +81,9 @@ def run_fm(fm, wl, m, q, k, v, dO=None, o_dtype=torch.float32, g_dtype=torch.flo
     lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
     fm.fm_attn_fwd(qd, kd, vd, att.bounds, att.plan, wl.scale, o, lse, att.status, flags=flags)
     out = dict(att=att, o=o, lse=lse)
+    torch.cuda.synchronize()
+    code = int(att.status.item())
+    assert code == 0, f"forward: device status {code} ({fm.fm_status_string(code)})"
     if dO is not None:
         dod = dO.to(dev)
         ws = torch.full((fm.fm_bwd_workspace_bytes(B, H, N, d),), 0xFF, dtype=torch.uint8, device=dev)
