@@ -101,9 +101,11 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, v
 // ---------------------------------------------------------------- main kernel
 template <int D, bool PRECISE>
 struct BwdSmem {
-    // Q/dO stages: three in standard mode; precise mode needs the room for
-    // the low operand terms and keeps two.
-    static constexpr int kStages = PRECISE ? 2 : 3;
+    // Two Q/dO stages.  Standard mode double-buffers the P^T/dS^T operand
+    // tiles (the P/dS warps write half i+1 while the products of half i still
+    // read half i); precise mode needs that room for the low operand terms.
+    static constexpr int kStages = 2;
+    static constexpr int kPBufs = PRECISE ? 1 : 2;
     static constexpr int kKBox = 128 * 128;     // 64 columns x 128 rows
     static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
     static constexpr int kKTile = 128 * D * 2;
@@ -112,23 +114,24 @@ struct BwdSmem {
     static constexpr int kK = 0, kV = kKTile;
     static constexpr int kQ = 2 * kKTile;                   // [kStages]
     static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
-    static constexpr int kP = kdO + kStages * kQTile;       // P^T  (high part)
-    static constexpr int kdS = kP + kOp;                    // dS^T (high part)
+    static constexpr int kP = kdO + kStages * kQTile;       // P^T  (high part)  [kPBufs]
+    static constexpr int kdS = kP + kOp;                    // dS^T (high part)  [kPBufs]
     static constexpr int kPlo = kdS + kOp;                  // precise: P^T low part
     static constexpr int kdSlo = kPlo + kOp;                // precise: dS^T low part
-    static constexpr int kDQ = PRECISE ? kdSlo + kOp : kPlo; // standard: fp32 dQ tile [32][D]
+    static constexpr int kPBufStride = 2 * kOp;             // standard: next (P^T, dS^T) pair
+    static constexpr int kDQ = PRECISE ? kdSlo + kOp : kP + 2 * kPBufStride; // standard: fp32 dQ tile [32][D]
     static constexpr int kList = PRECISE ? kDQ : kDQ + 32 * D * 4;
     static constexpr int kListCap = 2048;                   // Q tiles staged from the plan
     static constexpr int kStat = kList + kListCap * 4;      // lse2 [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
-    static constexpr int kNumBar = 20;
+    static constexpr int kNumBar = 21;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
 };
 
 enum {
-    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF, BB_SE, BB_PF, BB_DSE, BB_DQF0,
+    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF, BB_SE, BB_PF, BB_DSE0, BB_DSE1, BB_DQF0,
     BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_STF, BB_STE
 };
 
@@ -162,9 +165,12 @@ __global__ void __launch_bounds__(480, 1)
 {
     using S = BwdSmem<D, PRECISE>;
     constexpr int NBOX = D / 64;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // The kernel has no static shared memory, so the dynamic window starts on
+    // a 1024-byte boundary (checked below).  Pointers stay derived from the
+    // __shared__ array itself, so every access compiles to a shared-memory
+    // instruction rather than a generic one.
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
     uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
     uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS, *sPlo = smem + S::kPlo, *sdSlo = smem + S::kdSlo;
@@ -192,7 +198,9 @@ __global__ void __launch_bounds__(480, 1)
         const bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
                         ph->bq == 128 && ph->bk == 128;
         if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
-        *ok_sh = ok;
+        const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
+        if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
+        *ok_sh = ok && aligned;
         *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)sidx * L.n_k + kt] : 0;
         *abort = 0;
         mbar_init(&bars[BB_KV], 1);
@@ -203,7 +211,8 @@ __global__ void __launch_bounds__(480, 1)
         mbar_init(&bars[BB_SF], 1);
         mbar_init(&bars[BB_SE], 256);
         mbar_init(&bars[BB_PF], 256);
-        mbar_init(&bars[BB_DSE], 1);
+        mbar_init(&bars[BB_DSE0], 1);
+        mbar_init(&bars[BB_DSE1], 1);
         mbar_init(&bars[BB_DQF0], 1);
         mbar_init(&bars[BB_DQF1], 1);
         mbar_init(&bars[BB_DQE0], 128);
@@ -346,26 +355,28 @@ __global__ void __launch_bounds__(480, 1)
                         tc_fence_after();
                         const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
                         const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
+                        const int pb = (S::kPBufs == 2) ? (it & 1) : 0;   // P/dS buffer of this half
+                        const uint32_t pbo = pb * S::kPBufStride;
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                mma_ss(tdV, sdesc_add(dP[part], pbo + kk * 32), sdesc_add(dOm, kk * 2048), idKV,
                                        (it > 0 || part > 0 || kk > 0));
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdK, sdesc_add(dSk[part], kk * 32), sdesc_add(dQm, kk * 2048), idKV,
+                                mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
                                        (it > 0 || part > 0 || kk > 0));
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)
-                                mma_ss(tdQ + qb * 64, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], kk * 2048), idQ,
+                                mma_ss(tdQ + qb * 64, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048), idQ,
                                        (part > 0 || kk > 0));
                         tc_commit(&bars[BB_DQF0 + qb]);
-                        tc_commit(&bars[BB_DSE]);
+                        tc_commit(&bars[BB_DSE0 + pb]);
                         tc_commit(&bars[BB_QE0 + st]);
                     }
                 }
@@ -400,8 +411,14 @@ __global__ void __launch_bounds__(480, 1)
                 if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
                     !warp_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status)) { ok = false; break; }
                 tc_fence_after();
-                const float *l2 = sLse + st * 64 + c0;
-                const float *dd = sD + st * 64 + c0;
+                float l2[32], dd[32];
+#pragma unroll
+                for (int v4 = 0; v4 < 8; ++v4) {
+                    const float4 x = reinterpret_cast<const float4 *>(sLse + st * 64 + c0)[v4];
+                    const float4 y = reinterpret_cast<const float4 *>(sD + st * 64 + c0)[v4];
+                    l2[4 * v4] = x.x; l2[4 * v4 + 1] = x.y; l2[4 * v4 + 2] = x.z; l2[4 * v4 + 3] = x.w;
+                    dd[4 * v4] = y.x; dd[4 * v4 + 1] = y.y; dd[4 * v4 + 2] = y.z; dd[4 * v4 + 3] = y.w;
+                }
                 uint32_t sraw[32], draw[32];
                 tmem_ld32(tS + lane_off + c0, sraw);
                 tmem_ld32(tdP + lane_off + c0, draw);
@@ -423,7 +440,12 @@ __global__ void __launch_bounds__(480, 1)
                     p[c] = pv;
                     ds[c] = pv * (__uint_as_float(draw[c]) - dd[c]);
                 }
-                if (it > 0 && !warp_wait(&bars[BB_DSE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+                // The P/dS buffer of this half is free once the products of the
+                // half that last used it have completed.
+                const int pb = (S::kPBufs == 2) ? (it & 1) : 0;
+                const int back = S::kPBufs;                  // halves between two uses of a buffer
+                if (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status)) { ok = false; break; }
+                uint8_t *bP = sP + pb * S::kPBufStride, *bdS = sdS + pb * S::kPBufStride;
                 // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -441,8 +463,8 @@ __global__ void __launch_bounds__(480, 1)
                             dh[w2] = pack_bf16x2(ds[c], ds[c + 1]);
                         }
                     }
-                    *reinterpret_cast<uint4 *>(sP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                    *reinterpret_cast<uint4 *>(sdS + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
+                    *reinterpret_cast<uint4 *>(bP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                    *reinterpret_cast<uint4 *>(bdS + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
                     if (PRECISE) {
                         *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
                         *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);

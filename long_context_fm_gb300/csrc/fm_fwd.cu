@@ -90,9 +90,12 @@ __global__ void __launch_bounds__(352, 1)
 {
     using S = FwdSmem<D>;
     constexpr int NBOX = D / 64;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // The kernel has no static shared memory, so the dynamic window starts on
+    // a 1024-byte boundary (checked below).  Pointers stay derived from the
+    // __shared__ array itself, so every access compiles to a shared-memory
+    // instruction rather than a generic one.
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw;
     int4 *sBnd = reinterpret_cast<int4 *>(smem + S::kBnd);
     int32_t *sList0 = reinterpret_cast<int32_t *>(smem + S::kList0);
     int32_t *sList1 = reinterpret_cast<int32_t *>(smem + S::kList1);
@@ -117,7 +120,9 @@ __global__ void __launch_bounds__(352, 1)
         const bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
                         ph->bq == 128 && ph->bk == 128;
         if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
-        *ok_sh = ok;
+        const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
+        if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
+        *ok_sh = ok && aligned;
         const int32_t *rc = reinterpret_cast<const int32_t *>(a.plan + L.off_row_cnt) + (int64_t)sidx * L.n_q;
         cnt_sh[0] = ok ? rc[qt0] : 0;
         cnt_sh[1] = (ok && has1) ? rc[qt0 + 1] : 0;
