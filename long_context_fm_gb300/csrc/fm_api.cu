@@ -25,7 +25,7 @@ fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float sca
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const FwdArgs &a, int d, bool precise, cudaStream_t stream);
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a, int d,
+                             const CUtensorMap &tdo, const BwdArgs &a, int d,
                              bool precise, cudaStream_t stream);
 
 namespace {
@@ -62,22 +62,6 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, int BH, int N, int d, in
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// fp32 [BH, N, d] viewed as 3-D (d, N, BH); box = d columns x `rows` rows,
-// no swizzle (the row-major staging tile of a bulk reduce-add).
-bool make_tmap_f32_rows(CUtensorMap *map, const void *base, int BH, int N, int d, int rows)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-    const cuuint32_t box[3] = {(cuuint32_t)d, (cuuint32_t)rows, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
-                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -280,11 +264,10 @@ fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o
     if (!plan_layout(B, m.Hm, N, 128, 128, &L)) return FM_ERR_INVALID_ARG;
     if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
     if ((st = check_device()) != FM_OK) return st;
-    CUtensorMap tq, tk, tv, tdo, tdq;
+    CUtensorMap tq, tk, tv, tdo;
     float *dq_acc = reinterpret_cast<float *>(ws);
     if (!make_tmap_bf16(&tq, q, B * H, N, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
-        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, N, d, 64) ||
-        !make_tmap_f32_rows(&tdq, dq_acc, B * H, N, d, 32))
+        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, N, d, 64))
         return FM_ERR_CUDA;
     float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * N * d * 4));
     const int64_t rows = (int64_t)B * H * N;
@@ -298,7 +281,7 @@ fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o
     a.B = B; a.H = H; a.Hm = m.Hm; a.N = N;
     a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.g_f32 = grad_dtype == FM_DT_F32;
-    if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, tdq, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
+    if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
         return st;
     return fm_bwd_post_launch(dq_acc, dq, grad_dtype == FM_DT_F32, scale, rows * d, s);
 }

@@ -10,23 +10,27 @@
 // Main kernel: one CTA = one (b, h, 128-row KV tile); it walks the plan's
 // list of non-skip Q tiles of that KV tile (staged in shared memory), each as
 // two 64-row halves.
-//   warp 0      TMA producer (K and V once; Q, dO halves double-buffered;
-//               lse and D staged into shared memory by the whole warp)
+//   warp 0      TMA producer (K and V once; Q, dO halves in a ring of three
+//               stages, two in precise mode; lse and D staged into shared
+//               memory by the whole warp)
 //   warp 1      TMEM allocation; one thread issues the score MMAs (S^T, dP^T)
-//   warps 2-9   two warpgroups, one thread per KV row j each: P^T and dS^T
-//               for columns [0, 32) and [32, 64) of the half
-//   warps 10-13 one thread per head-dim index: drain dQ^T from TMEM into the
-//               fp32 dQ accumulator (standard mode: shared-memory tile plus a
-//               bulk tensor reduce-add; precise mode: red.global.add)
-//   warp 14     one thread issues the gradient MMAs (dV, dK, dQ^T)
-// TMEM (512 columns): dK [0, d), dV [128, 128 + d), S^T [256, 320),
-// dP^T [320, 384), dQ^T [384, 448).  Per half (M = 128 KV rows):
+//   warps 2-17  four warpgroups, one thread per KV row j each: P^T and dS^T
+//               for 16 of the half's 64 columns each
+//   warps 18-21 one thread per head-dim index: drain dQ^T from TMEM into the
+//               fp32 dQ accumulator with red.global.add
+//   warp 22     one thread issues the gradient MMAs (dV, dK, dQ^T)
+// TMEM (512 columns): dK [0, d), dV [128, 128 + d), two score buffers
+// b = half & 1 with S^T [256 + 128 b, +64) and dP^T [320 + 128 b, +64); the
+// half's dQ^T lands in the S^T columns after P^T/dS^T are written, so the
+// scores of the next half run while this half is still being processed.
+// Per half (M = 128 KV rows):
 //   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
 //   dP^T = V dO^T       (SS, K-major/K-major)        -> TMEM
 //   P^T  = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T o (dP^T - D)
-//          each written as two bf16 terms (hi + lo, ~16 significant bits)
-//          into 128-byte-swizzled shared memory; the MMAs below consume both
-//          terms, so the gradients do not carry a bf16 rounding of P or dS
+//          written as bf16 into 128-byte-swizzled shared memory (precise
+//          mode: as two bf16 terms hi + lo, ~16 significant bits, both
+//          consumed by the MMAs below, so the gradients do not carry a bf16
+//          rounding of P or dS)
 //   dV  += P^T dO       (SS, P^T K-major, dO MN-major)
 //   dK  += dS^T Q       (SS, dS^T K-major, Q MN-major)
 //   dQ^T = K^T dS^T     (SS, K MN-major, dS^T MN-major)
@@ -101,11 +105,13 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, v
 // ---------------------------------------------------------------- main kernel
 template <int D, bool PRECISE>
 struct BwdSmem {
-    // Two Q/dO stages.  Standard mode double-buffers the P^T/dS^T operand
-    // tiles (the P/dS warps write half i+1 while the products of half i still
-    // read half i); precise mode needs that room for the low operand terms.
-    static constexpr int kStages = 2;
-    static constexpr int kPBufs = PRECISE ? 1 : 2;
+    // Standard mode: three Q/dO stages (a stage's next load is in flight
+    // while the two halves before it are processed), one P^T tile (free as
+    // soon as dV has read it) and two dS^T tiles (dK and dQ^T of half i still
+    // read dS^T while half i+1 is written).  Precise mode keeps two stages and
+    // single operand tiles: the low operand terms take that room.
+    static constexpr int kStages = PRECISE ? 2 : 3;
+    static constexpr int kdSBufs = PRECISE ? 1 : 2;
     static constexpr int kKBox = 128 * 128;     // 64 columns x 128 rows
     static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
     static constexpr int kKTile = 128 * D * 2;
@@ -114,14 +120,12 @@ struct BwdSmem {
     static constexpr int kK = 0, kV = kKTile;
     static constexpr int kQ = 2 * kKTile;                   // [kStages]
     static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
-    static constexpr int kP = kdO + kStages * kQTile;       // P^T  (high part)  [kPBufs]
-    static constexpr int kdS = kP + kOp;                    // dS^T (high part)  [kPBufs]
-    static constexpr int kPlo = kdS + kOp;                  // precise: P^T low part
+    static constexpr int kP = kdO + kStages * kQTile;       // P^T  (high part)
+    static constexpr int kdS = kP + kOp;                    // dS^T (high part)  [kdSBufs]
+    static constexpr int kPlo = kdS + kdSBufs * kOp;        // precise: P^T low part
     static constexpr int kdSlo = kPlo + kOp;                // precise: dS^T low part
-    static constexpr int kPBufStride = 2 * kOp;             // standard: next (P^T, dS^T) pair
-    static constexpr int kDQ = PRECISE ? kdSlo + kOp : kP + 2 * kPBufStride; // standard: fp32 dQ tile [32][D]
-    static constexpr int kList = PRECISE ? kDQ : kDQ + 32 * D * 4;
-    static constexpr int kListCap = 2048;                   // Q tiles staged from the plan
+    static constexpr int kList = PRECISE ? kdSlo + kOp : kPlo;
+    static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
     static constexpr int kStat = kList + kListCap * 4;      // lse2 [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
     static constexpr int kNumBar = 21;
@@ -131,8 +135,8 @@ struct BwdSmem {
 };
 
 enum {
-    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF, BB_SE, BB_PF, BB_DSE0, BB_DSE1, BB_DQF0,
-    BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_STF, BB_STE
+    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_PF0, BB_PF1, BB_PE, BB_DSE0,
+    BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1
 };
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
@@ -144,24 +148,12 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
     lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
 }
 
-// Bulk reduce-add of a row-major fp32 shared-memory tile into global memory
-// through a tensor map (no multicast); completion tracked by a bulk group.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
-{
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D, bool PRECISE>
-__global__ void __launch_bounds__(480, 1)
+__global__ void __launch_bounds__(736, 1)
     fm_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const __grid_constant__ CUtensorMap tdq, const BwdArgs a)
+                  const BwdArgs a)
 {
     using S = BwdSmem<D, PRECISE>;
     constexpr int NBOX = D / 64;
@@ -174,7 +166,6 @@ __global__ void __launch_bounds__(480, 1)
     uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
     uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
     uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS, *sPlo = smem + S::kPlo, *sdSlo = smem + S::kdSlo;
-    float *sDQ = reinterpret_cast<float *>(smem + S::kDQ);
     int32_t *sList = reinterpret_cast<int32_t *>(smem + S::kList);
     constexpr int NST = S::kStages;
     float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [NST][64]
@@ -208,9 +199,11 @@ __global__ void __launch_bounds__(480, 1)
             mbar_init(&bars[BB_QF0 + s2], 33);
             mbar_init(&bars[BB_QE0 + s2], 2);     // scores and gradients issuers
         }
-        mbar_init(&bars[BB_SF], 1);
-        mbar_init(&bars[BB_SE], 256);
-        mbar_init(&bars[BB_PF], 256);
+        mbar_init(&bars[BB_SF0], 1);
+        mbar_init(&bars[BB_SF1], 1);
+        mbar_init(&bars[BB_PF0], 512);    // four P/dS warpgroups
+        mbar_init(&bars[BB_PF1], 512);
+        mbar_init(&bars[BB_PE], 1);
         mbar_init(&bars[BB_DSE0], 1);
         mbar_init(&bars[BB_DSE1], 1);
         mbar_init(&bars[BB_DQF0], 1);
@@ -220,8 +213,6 @@ __global__ void __launch_bounds__(480, 1)
         mbar_init(&bars[BB_ACC], 1);
         mbar_init(&bars[BB_DRAIN0], 1);
         mbar_init(&bars[BB_DRAIN1], 1);
-        mbar_init(&bars[BB_STF], 128);
-        mbar_init(&bars[BB_STE], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -233,7 +224,9 @@ __global__ void __launch_bounds__(480, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     // TMEM: dK, dV, S^T, dP^T, and dQ^T double-buffered (half it uses buffer it & 1).
-    const uint32_t tdK = tmem, tdV = tmem + 128, tS = tmem + 256, tdP = tmem + 320, tdQ = tmem + 384;
+    // Score buffer b = half & 1: S^T at 256 + 128 b, dP^T at 320 + 128 b; the
+    // half's dQ^T reuses the S^T columns once P^T/dS^T have been written.
+    const uint32_t tdK = tmem, tdV = tmem + 128, tS0 = tmem + 256, tdP0 = tmem + 320;
     const int cnt = *cnt_sh;
     const int32_t *glist =
         reinterpret_cast<const int32_t *>(a.plan + L.off_col_list) + ((int64_t)sidx * L.n_k + kt) * L.n_q;
@@ -300,11 +293,11 @@ __global__ void __launch_bounds__(480, 1)
                 for (int k2 = (it > NST ? it - NST : 0); k2 < it; ++k2)
                     mbar_wait_drain(&bars[BB_QF0 + (k2 % NST)], (k2 / NST) & 1, a.status);
             }
-        } else if (warp == 1 || warp == 14) {
+        } else if (warp == 1 || warp == 22) {
             // ------------------------------------------------ MMA issuers
             // Two issuing threads: warp 1 issues the scores S^T, dP^T of each
             // half as soon as its Q/dO have landed and the S buffer is drained;
-            // warp 14 issues the gradient products dV, dK, dQ^T of each half as
+            // warp 22 issues the gradient products dV, dK, dQ^T of each half as
             // soon as its P/dS are written.  Each blocks on the tensor-core
             // queue independently, so the next scores are never held back
             // behind the current gradients (or the reverse).  A Q/dO stage is
@@ -328,56 +321,62 @@ __global__ void __launch_bounds__(480, 1)
                     const uint64_t dQk = sdesc_sw128(smem_u32(sQ + st * S::kQTile), 16, 1024);
                     const uint64_t dOk = sdesc_sw128(smem_u32(sdO + st * S::kQTile), 16, 1024);
                     if (scores) {
+                        const int b = it & 1;
+                        // Buffer b is free once the drain holds the dQ^T of the half
+                        // that used it before (which also implies its S^T, dP^T were read).
                         if (!mbar_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status) ||
-                            (it > 0 && !mbar_wait(&bars[BB_SE], (it - 1) & 1, abort, a.status))) { ok = false; break; }
+                            (it >= 2 && !mbar_wait(&bars[BB_DQE0 + b], ((it >> 1) - 1) & 1, abort, a.status))) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tS, sdesc_add(dKk, ok_), sdesc_add(dQk, oq), idS, kk > 0);
+                            mma_ss(tS0 + b * 128, sdesc_add(dKk, ok_), sdesc_add(dQk, oq), idS, kk > 0);
                         }
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tdP, sdesc_add(dVk, ok_), sdesc_add(dOk, oq), idS, kk > 0);
+                            mma_ss(tdP0 + b * 128, sdesc_add(dVk, ok_), sdesc_add(dOk, oq), idS, kk > 0);
                         }
-                        tc_commit(&bars[BB_SF]);
+                        tc_commit(&bars[BB_SF0 + b]);
                         tc_commit(&bars[BB_QE0 + st]);
                     } else {
-                        const int qb = it & 1;         // dQ^T buffer
-                        if (!mbar_wait(&bars[BB_PF], it & 1, abort, a.status) ||
-                            (it >= 2 && !mbar_wait(&bars[BB_DQE0 + qb], ((it >> 1) - 1) & 1, abort, a.status))) {
+                        const int qb = it & 1;         // score buffer: dQ^T goes into its S^T columns
+                        if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
                         const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
-                        const int pb = (S::kPBufs == 2) ? (it & 1) : 0;   // P/dS buffer of this half
-                        const uint32_t pbo = pb * S::kPBufStride;
+                        const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;   // dS^T buffer of this half
+                        const uint32_t pbo = pb * S::kOp;
+                        // Each commit releases its inputs as early as possible: P^T
+                        // after dV, the Q/dO stage after dK, dS^T and the score
+                        // buffer (now holding dQ^T) after dQ^T.
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdV, sdesc_add(dP[part], pbo + kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
                                        (it > 0 || part > 0 || kk > 0));
+                        tc_commit(&bars[BB_PE]);
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
                                        (it > 0 || part > 0 || kk > 0));
+                        tc_commit(&bars[BB_QE0 + st]);
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)
-                                mma_ss(tdQ + qb * 64, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048), idQ,
+                                mma_ss(tS0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048), idQ,
                                        (part > 0 || kk > 0));
                         tc_commit(&bars[BB_DQF0 + qb]);
                         tc_commit(&bars[BB_DSE0 + pb]);
-                        tc_commit(&bars[BB_QE0 + st]);
                     }
                 }
                 if (ok && !scores) tc_commit(&bars[BB_ACC]);
@@ -386,14 +385,15 @@ __global__ void __launch_bounds__(480, 1)
                 tc_commit(&bars[BB_DRAIN0 + (scores ? 0 : 1)]);
                 mbar_wait_drain(&bars[BB_DRAIN0 + (scores ? 0 : 1)], 0, a.status);
             }
-        } else if (warp < 10) {
+        } else if (warp < 18) {
             // ------------------------------------------------ P^T / dS^T
-            // Two warpgroups: warps 2-5 take columns [0, 32) of each half,
-            // warps 6-9 columns [32, 64); thread = KV row (TMEM lane).
+            // Four warpgroups (warps 2-5, 6-9, 10-13, 14-17) take 16 columns of
+            // each half each; thread = KV row (TMEM lane).
+            constexpr int CW = 16;                   // columns per thread
+            const int wg = (warp - 2) >> 2;
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;       // KV row within the tile
-            const int c0 = (warp < 6) ? 0 : 32;      // first column of this warpgroup
-            const bool first_wg = warp < 6;
+            const int c0 = wg * CW;                  // first column of this warpgroup
             const int j = kb + r;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             int lo0 = 0, lolen = 0, up0 = 0, uplen = 0x7fffffff;   // beyond N: masked everywhere
@@ -408,28 +408,27 @@ __global__ void __launch_bounds__(480, 1)
                 const int q0 = q0_of(it);
                 const bool pred = ((entry(it >> 1) >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
                 const int st = it % NST;
-                if (!warp_wait(&bars[BB_SF], it & 1, abort, a.status) ||
+                const int b = it & 1;                     // score buffer
+                if (!warp_wait(&bars[BB_SF0 + b], (it >> 1) & 1, abort, a.status) ||
                     !warp_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status)) { ok = false; break; }
                 tc_fence_after();
-                float l2[32], dd[32];
+                uint32_t sraw[CW], draw[CW];
+                tmem_ld16(tS0 + b * 128 + lane_off + c0, sraw);
+                tmem_ld16(tdP0 + b * 128 + lane_off + c0, draw);
+                float l2[CW], dd[CW];
 #pragma unroll
-                for (int v4 = 0; v4 < 8; ++v4) {
+                for (int v4 = 0; v4 < CW / 4; ++v4) {
                     const float4 x = reinterpret_cast<const float4 *>(sLse + st * 64 + c0)[v4];
                     const float4 y = reinterpret_cast<const float4 *>(sD + st * 64 + c0)[v4];
                     l2[4 * v4] = x.x; l2[4 * v4 + 1] = x.y; l2[4 * v4 + 2] = x.z; l2[4 * v4 + 3] = x.w;
                     dd[4 * v4] = y.x; dd[4 * v4 + 1] = y.y; dd[4 * v4 + 2] = y.z; dd[4 * v4 + 3] = y.w;
                 }
-                uint32_t sraw[32], draw[32];
-                tmem_ld32(tS + lane_off + c0, sraw);
-                tmem_ld32(tdP + lane_off + c0, draw);
                 tmem_ld_wait();
                 tmem_reg_fence(sraw);
                 tmem_reg_fence(draw);
-                tc_fence_before();
-                mbar_arrive(&bars[BB_SE]);      // this warpgroup's half of S^T, dP^T is in registers
-                float p[32], ds[32];
+                float p[CW], ds[CW];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int c = 0; c < CW; ++c) {
                     float pv = ex2(fmaf(__uint_as_float(sraw[c]), a.scale_log2, -l2[c]));
                     if (pred) {
                         const int qi = q0 + c0 + c;
@@ -440,15 +439,17 @@ __global__ void __launch_bounds__(480, 1)
                     p[c] = pv;
                     ds[c] = pv * (__uint_as_float(draw[c]) - dd[c]);
                 }
-                // The P/dS buffer of this half is free once the products of the
-                // half that last used it have completed.
-                const int pb = (S::kPBufs == 2) ? (it & 1) : 0;
-                const int back = S::kPBufs;                  // halves between two uses of a buffer
-                if (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status)) { ok = false; break; }
-                uint8_t *bP = sP + pb * S::kPBufStride, *bdS = sdS + pb * S::kPBufStride;
+                // P^T is free once dV of the previous half has read it; this
+                // half's dS^T buffer once dK, dQ^T of the half that last used
+                // it have completed.
+                const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;
+                const int back = S::kdSBufs;                 // halves between two uses of a dS^T buffer
+                if ((it >= 1 && !warp_wait(&bars[BB_PE], (it - 1) & 1, abort, a.status)) ||
+                    (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status))) { ok = false; break; }
+                uint8_t *bP = sP, *bdS = sdS + pb * S::kOp;
                 // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < CW / 8; ++u) {
                     const int chunk = (c0 >> 3) + u;
                     const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
                     uint32_t ph[4], pl[4], dh[4], dl[4];
@@ -471,22 +472,26 @@ __global__ void __launch_bounds__(480, 1)
                     }
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars[BB_PF]);
+                tc_fence_before();                  // S^T, dP^T reads of this half precede the dQ^T MMA
+                mbar_arrive(&bars[BB_PF0 + b]);
             }
             // ------------------------------------------------ dK, dV epilogue
-            // The first warpgroup stores dK, the second dV.
+            // Warpgroups 0, 1 store the two column halves of dK; 2, 3 of dV.
             if (ok && (n_it == 0 || warp_wait(&bars[BB_ACC], 0, abort, a.status))) {
                 tc_fence_after();
                 const bool row_in = j < N;
                 const int64_t row = (int64_t)bh * N + j;
-                const uint32_t tsrc = first_wg ? tdK : tdV;
-                const float mul = first_wg ? a.scale : 1.f;
-                void *dst = first_wg ? a.dk : a.dv;
+                const bool is_dk = wg < 2;
+                const uint32_t tsrc = is_dk ? tdK : tdV;
+                const float mul = is_dk ? a.scale : 1.f;
+                void *dst = is_dk ? a.dk : a.dv;
+                const int cbase = (wg & 1) * (D / 2);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    const int col = cbase + cc * 32;
                     uint32_t v[32];
                     if (n_it > 0) {            // warp-uniform: every lane loads
-                        tmem_ld32(tsrc + lane_off + c * 32, v);
+                        tmem_ld32(tsrc + lane_off + col, v);
                         tmem_ld_wait();
                         tmem_reg_fence(v);
                     } else {
@@ -495,13 +500,13 @@ __global__ void __launch_bounds__(480, 1)
                     }
                     if (!row_in) continue;
                     if (a.g_f32) {
-                        float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + c * 32);
+                        float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + col);
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
                             pp[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
                                                 __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
                     } else {
-                        uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + c * 32);
+                        uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + col);
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
                             pp[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
@@ -511,63 +516,38 @@ __global__ void __launch_bounds__(480, 1)
                     }
                 }
             }
-        } else if (warp < 14) {
+        } else if (warp < 22) {
             // ------------------------------------------------ dQ drain
-            // Thread = head-dim index (TMEM lane of dQ^T).  Standard mode:
-            // the 64 x d tile goes through a 32-row shared-memory tile and two
-            // bulk tensor reduce-adds per half; precise mode: coalesced
-            // red.global.add.
+            // Thread = head-dim index (TMEM lane of dQ^T).  The half's 64 x d
+            // tile goes from registers straight into the fp32 dQ accumulator
+            // with red.global.add (one coalesced 128-byte request per warp and
+            // row): the reductions need no staging and nothing waits for
+            // them, so the drain never holds the score buffer for longer
+            // than the two TMEM loads.
             const int quarter = warp & 3;
             const int dd = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-            const bool leader = (warp == 10 && lane == 0);
-            int sub = 0;   // staging-tile uses so far
+            const bool has_cols = quarter * 32 < D;          // warp-uniform
             for (int it = 0; it < n_it; ++it) {
                 const int q0 = q0_of(it);
                 const int qb = it & 1;
                 if (!warp_wait(&bars[BB_DQF0 + qb], (it >> 1) & 1, abort, a.status)) break;
                 tc_fence_after();
                 uint32_t v[2][32];
-                tmem_ld32(tdQ + qb * 64 + lane_off, v[0]);
-                tmem_ld32(tdQ + qb * 64 + lane_off + 32, v[1]);
+                tmem_ld32(tS0 + qb * 128 + lane_off, v[0]);
+                tmem_ld32(tS0 + qb * 128 + lane_off + 32, v[1]);
                 tmem_ld_wait();
-                tmem_reg_fence(v[0]); tmem_reg_fence(v[1]);
+                tmem_reg_fence(v[0]);
+                tmem_reg_fence(v[1]);
                 tc_fence_before();
-                mbar_arrive(&bars[BB_DQE0 + qb]);
-                if (PRECISE) {
-                    if (dd < D) {
-                        float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
-                        const int lim = min(64, N - q0);
+                mbar_arrive(&bars[BB_DQE0 + qb]);   // score buffer qb is free again
+                if (!has_cols) continue;
+                float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
+                const int lim = min(64, N - q0);       // rows beyond N: nothing to add
 #pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
-                    }
-                } else {
-                    bool okq = true;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh, ++sub) {
-                        if (q0 + hh * 32 >= N) break;            // rows beyond N: nothing to add
-                        if (sub > 0 && !warp_wait(&bars[BB_STE], (sub - 1) & 1, abort, a.status)) { okq = false; break; }
-                        if (dd < D) {
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) sDQ[c * D + dd] = __uint_as_float(v[hh][c]);
-                        }
-                        fence_proxy_async_smem();
-                        mbar_arrive(&bars[BB_STF]);
-                        if (leader) {
-                            // Rows beyond N are clipped by the tensor map.
-                            if (mbar_wait(&bars[BB_STF], sub & 1, abort, a.status)) {
-                                tma_reduce_add_3d(&tdq, sDQ, 0, q0 + hh * 32, bh);
-                                bulk_commit();
-                                bulk_wait_read0();
-                            }
-                            mbar_arrive(&bars[BB_STE]);
-                        }
-                    }
-                    if (!okq) break;
-                }
+                for (int c = 0; c < 64; ++c)
+                    if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
             }
-            if (!PRECISE && leader) bulk_wait0();   // reductions complete before exit
         }
     }
     tc_fence_before();
@@ -599,7 +579,7 @@ fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dou
 
 template <int D, bool PRECISE>
 static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a,
+                            const CUtensorMap &tdo, const BwdArgs &a,
                             cudaStream_t stream)
 {
     constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
@@ -608,19 +588,19 @@ static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
         cudaSuccess)
         return FM_ERR_CUDA;
     ProfScope ps(kKBwd, stream);
-    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 480, smem, stream>>>(tq, tk, tv, tdo, tdq, a);
+    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 736, smem, stream>>>(tq, tk, tv, tdo, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const CUtensorMap &tdo, const CUtensorMap &tdq, const BwdArgs &a, int d,
+                             const CUtensorMap &tdo, const BwdArgs &a, int d,
                              bool precise, cudaStream_t stream)
 {
     if (d == 128)
-        return precise ? launch_bwd<128, true>(tq, tk, tv, tdo, tdq, a, stream)
-                       : launch_bwd<128, false>(tq, tk, tv, tdo, tdq, a, stream);
-    return precise ? launch_bwd<64, true>(tq, tk, tv, tdo, tdq, a, stream)
-                   : launch_bwd<64, false>(tq, tk, tv, tdo, tdq, a, stream);
+        return precise ? launch_bwd<128, true>(tq, tk, tv, tdo, a, stream)
+                       : launch_bwd<128, false>(tq, tk, tv, tdo, a, stream);
+    return precise ? launch_bwd<64, true>(tq, tk, tv, tdo, a, stream)
+                   : launch_bwd<64, false>(tq, tk, tv, tdo, a, stream);
 }
 
 fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,
