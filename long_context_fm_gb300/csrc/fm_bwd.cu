@@ -126,7 +126,7 @@ struct BwdSmem {
     static constexpr int kdSlo = kPlo + kOp;                // precise: dS^T low part
     static constexpr int kList = PRECISE ? kdSlo + kOp : kPlo;
     static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
-    static constexpr int kStat = kList + kListCap * 4;      // lse2 [kStages][64], D [kStages][64]
+    static constexpr int kStat = kList + kListCap * 4;      // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
     static constexpr int kNumBar = 21;
     static constexpr int kMisc = kBar + kNumBar * 8;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(736, 1)
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int r = lane + rr * 32;
-                    sLse[st * 64 + r] = (lv[rr] == -INFINITY) ? INFINITY : lv[rr] * 1.4426950408889634f;
+                    sLse[st * 64 + r] = (lv[rr] == -INFINITY) ? -INFINITY : -lv[rr] * 1.4426950408889634f;
                     sD[st * 64 + r] = dv[rr];
                 }
                 mbar_arrive(&bars[BB_QF0 + st]);     // 32 arrivals after the stores (+1 expect_tx)
@@ -352,23 +352,11 @@ __global__ void __launch_bounds__(736, 1)
                         const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
                         const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;   // dS^T buffer of this half
                         const uint32_t pbo = pb * S::kOp;
-                        // Each commit releases its inputs as early as possible: P^T
-                        // after dV, the Q/dO stage after dK, dS^T and the score
-                        // buffer (now holding dQ^T) after dQ^T.
-#pragma unroll
-                        for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
-                                       (it > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[BB_PE]);
-#pragma unroll
-                        for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
-                                       (it > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[BB_QE0 + st]);
+                        // dQ^T first: the score buffer it lands in is the one the
+                        // scores of half it + 2 wait for.  Each commit releases its
+                        // inputs as early as possible: the score buffer (through the
+                        // drain) after dQ^T, dS^T after dK, P^T and the Q/dO stage
+                        // after dV.
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
@@ -376,7 +364,21 @@ __global__ void __launch_bounds__(736, 1)
                                 mma_ss(tS0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048), idQ,
                                        (part > 0 || kk > 0));
                         tc_commit(&bars[BB_DQF0 + qb]);
+#pragma unroll
+                        for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
+                                       (it > 0 || part > 0 || kk > 0));
                         tc_commit(&bars[BB_DSE0 + pb]);
+#pragma unroll
+                        for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                       (it > 0 || part > 0 || kk > 0));
+                        tc_commit(&bars[BB_PE]);
+                        tc_commit(&bars[BB_QE0 + st]);
                     }
                 }
                 if (ok && !scores) tc_commit(&bars[BB_ACC]);
@@ -415,29 +417,40 @@ __global__ void __launch_bounds__(736, 1)
                 uint32_t sraw[CW], draw[CW];
                 tmem_ld16(tS0 + b * 128 + lane_off + c0, sraw);
                 tmem_ld16(tdP0 + b * 128 + lane_off + c0, draw);
-                float l2[CW], dd[CW];
+                // -lse*log2e and D of this warpgroup's columns, as packed pairs.
+                uint64_t nl2[CW / 2], dd2[CW / 2];
 #pragma unroll
                 for (int v4 = 0; v4 < CW / 4; ++v4) {
                     const float4 x = reinterpret_cast<const float4 *>(sLse + st * 64 + c0)[v4];
                     const float4 y = reinterpret_cast<const float4 *>(sD + st * 64 + c0)[v4];
-                    l2[4 * v4] = x.x; l2[4 * v4 + 1] = x.y; l2[4 * v4 + 2] = x.z; l2[4 * v4 + 3] = x.w;
-                    dd[4 * v4] = y.x; dd[4 * v4 + 1] = y.y; dd[4 * v4 + 2] = y.z; dd[4 * v4 + 3] = y.w;
+                    nl2[2 * v4] = f2_pack(x.x, x.y); nl2[2 * v4 + 1] = f2_pack(x.z, x.w);
+                    dd2[2 * v4] = f2_pack(y.x, y.y); dd2[2 * v4 + 1] = f2_pack(y.z, y.w);
                 }
                 tmem_ld_wait();
                 tmem_reg_fence(sraw);
                 tmem_reg_fence(draw);
+                // Column pairs in packed fp32: x = S*scale*log2e - lse*log2e,
+                // P = exp2(x), dS = P (dP - D).
                 float p[CW], ds[CW];
+                const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
 #pragma unroll
-                for (int c = 0; c < CW; ++c) {
-                    float pv = ex2(fmaf(__uint_as_float(sraw[c]), a.scale_log2, -l2[c]));
+                for (int c = 0; c < CW; c += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1])), sc2, nl2[c / 2]), x0, x1);
+                    float p0 = ex2(x0), p1 = ex2(x1);
                     if (pred) {
                         const int qi = q0 + c0 + c;
-                        const bool msk = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
-                                         ((unsigned)(qi - up0) < (unsigned)uplen);
-                        pv = msk ? 0.f : pv;
+                        const bool m0 = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
+                                        ((unsigned)(qi - up0) < (unsigned)uplen);
+                        const bool m1 = ((unsigned)(qi + 1 - lo0) < (unsigned)lolen) ||
+                                        ((unsigned)(qi + 1 - up0) < (unsigned)uplen);
+                        p0 = m0 ? 0.f : p0;
+                        p1 = m1 ? 0.f : p1;
                     }
-                    p[c] = pv;
-                    ds[c] = pv * (__uint_as_float(draw[c]) - dd[c]);
+                    p[c] = p0;
+                    p[c + 1] = p1;
+                    const uint64_t t2 = f2_sub(f2_pack(__uint_as_float(draw[c]), __uint_as_float(draw[c + 1])), dd2[c / 2]);
+                    f2_unpack(f2_mul(f2_pack(p0, p1), t2), ds[c], ds[c + 1]);
                 }
                 // P^T is free once dV of the previous half has read it; this
                 // half's dS^T buffer once dK, dQ^T of the half that last used
