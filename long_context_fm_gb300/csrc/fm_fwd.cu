@@ -50,7 +50,7 @@ struct FwdSmem {
     static constexpr int kList0 = kBnd + 4096;
     static constexpr int kList1 = kList0 + kListCap * 4;
     static constexpr int kBar = kList1 + kListCap * 4;
-    static constexpr int kNumBar = 20;
+    static constexpr int kNumBar = 22;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
@@ -58,7 +58,7 @@ struct FwdSmem {
 
 enum {
     FB_Q = 0, FB_KF0, FB_KF1, FB_KE0, FB_KE1, FB_VF0, FB_VF1, FB_VE0, FB_VE1, FB_BF0, FB_BF1,
-    FB_S0, FB_S1, FB_P0, FB_P1, FB_O0, FB_O1, FB_DRAIN0, FB_DRAIN1
+    FB_S0, FB_S1, FB_P0, FB_P1, FB_O0, FB_O1, FB_DRAIN0, FB_DRAIN1, FB_TK0, FB_TK1
 };
 
 // Walks the union of two ascending lists of KV tiles (entries tile | label << 28).
@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(352, 1)
         }
         mbar_init(&bars[FB_DRAIN0], 1);
         mbar_init(&bars[FB_DRAIN1], 1);
+        mbar_init(&bars[FB_TK0], 128);   // exponential-phase token for softmax 0 / 1
+        mbar_init(&bars[FB_TK1], 128);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -309,8 +311,24 @@ __global__ void __launch_bounds__(352, 1)
             int cnt = 0;
             bool done = true;
             int t = 0, kt, lab[2];
+            // The two softmax warpgroups take turns on the exponential phase
+            // (MUFU), tile by tile of the union walk: 0 runs tile t after 1
+            // has finished (or skipped) tile t - 1, and 1 runs tile t after 0
+            // has finished (or skipped) tile t.  While one exponentiates, the
+            // tensor core runs the other stream's products.  A warpgroup
+            // always waits for its turn before handing it on, so neither
+            // token barrier runs more than one phase ahead of its waiter.
+            auto take_turn = [&](int tt) {
+                if (q == 0) return tt == 0 || warp_wait(&bars[FB_TK0], (tt - 1) & 1, abort, a.status);
+                return warp_wait(&bars[FB_TK1], tt & 1, abort, a.status);
+            };
+            auto pass_turn = [&]() { mbar_arrive(&bars[q == 0 ? FB_TK1 : FB_TK0]); };
             for (; walk.next(kt, lab[0], lab[1]); ++t) {
-                if (lab[q] < 0) continue;
+                if (lab[q] < 0) {
+                    if (!take_turn(t)) { done = false; break; }
+                    pass_turn();
+                    continue;
+                }
                 const int st = t & 1;
                 const bool pred = (lab[q] == FM_TILE_PARTIAL) || (kt * 128 + 128 > N);
                 if (!warp_wait(&bars[FB_S0 + q], cnt & 1, abort, a.status)) { done = false; break; }
@@ -334,51 +352,55 @@ __global__ void __launch_bounds__(352, 1)
                         sv[cc] = msk ? -INFINITY : sv[cc];
                     }
                 }
-                float mx0 = sv[0], mx1 = sv[1], mx2 = sv[2], mx3 = sv[3];
+                float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
 #pragma unroll
-                for (int cc = 4; cc < 128; cc += 4) {
-                    mx0 = fmaxf(mx0, sv[cc]);
-                    mx1 = fmaxf(mx1, sv[cc + 1]);
-                    mx2 = fmaxf(mx2, sv[cc + 2]);
-                    mx3 = fmaxf(mx3, sv[cc + 3]);
-                }
-                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * a.scale_log2;   // -inf stays -inf
+                for (int k2 = 0; k2 < 62; ++k2) mx4[k2 & 3] = fmax3(mx4[k2 & 3], sv[4 + 2 * k2], sv[5 + 2 * k2]);
+                const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;   // -inf stays -inf
                 float m_new = m, alpha = 1.f;
                 if (mx > m + 8.f) {
                     m_new = mx;
                     alpha = ex2(m - m_new);                  // m = -inf gives 0
                 }
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+                if (!take_turn(t)) { done = false; break; }
                 // P = exp2(s * scale*log2e - m), written over S as packed bf16.
                 // Precise mode: two terms, P_hi = bf16(P) in columns [0, 64) and
                 // P_lo = bf16(P - P_hi) in columns [64, 128).  Standard mode:
                 // P_hi only, and O is normalised by the sum of the rounded P,
                 // i.e. of the weights the PV product really applied, so the
                 // normalised weights sum to one.  lse uses the fp32 sum.
-                float sum0 = 0.f, sum1 = 0.f, rs0 = 0.f, rs1 = 0.f;
+                // Column pairs in packed fp32: x = s * scale*log2e - m, and the
+                // running sums of P and of the rounded P.
+                const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-m_use, -m_use);
+                uint64_t sum2 = f2_pack(0.f, 0.f), rs2 = f2_pack(0.f, 0.f);
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) {
-                        const float p0 = ex2(fmaf(sv[hh * 32 + 2 * cc], a.scale_log2, -m_use));
-                        const float p1 = ex2(fmaf(sv[hh * 32 + 2 * cc + 1], a.scale_log2, -m_use));
-                        sum0 += p0;
-                        sum1 += p1;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(sv[hh * 32 + 2 * cc], sv[hh * 32 + 2 * cc + 1]), sc2, nm2), x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        sum2 = f2_add(sum2, f2_pack(p0, p1));
                         hi[cc] = pack_bf16x2(p0, p1);
                         if (PRECISE) {
                             lo[cc] = pack_bf16x2(p0 - __uint_as_float(hi[cc] << 16),
                                                  p1 - __uint_as_float(hi[cc] & 0xffff0000u));
                         } else {
-                            rs0 += __uint_as_float(hi[cc] << 16);
-                            rs1 += __uint_as_float(hi[cc] & 0xffff0000u);
+                            rs2 = f2_add(rs2, f2_pack(__uint_as_float(hi[cc] << 16), __uint_as_float(hi[cc] & 0xffff0000u)));
                         }
                     }
                     tmem_st16(tS + lane_off + hh * 16, hi);
                     if (PRECISE) tmem_st16(tS + lane_off + 64 + hh * 16, lo);
                 }
-                l = l * alpha + (sum0 + sum1);
-                if (!PRECISE) lr = lr * alpha + (rs0 + rs1);
+                pass_turn();
+                float s0, s1;
+                f2_unpack(sum2, s0, s1);
+                l = l * alpha + (s0 + s1);
+                if (!PRECISE) {
+                    f2_unpack(rs2, s0, s1);
+                    lr = lr * alpha + (s0 + s1);
+                }
                 m = m_new;
                 // Rescale O when the max moved (O holds this tile's earlier KV
                 // tiles; their PV finished before this S was computed).
