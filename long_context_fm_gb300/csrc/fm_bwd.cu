@@ -353,10 +353,11 @@ __global__ void __launch_bounds__(736, 1)
                         const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;   // dS^T buffer of this half
                         const uint32_t pbo = pb * S::kOp;
                         // dQ^T first: the score buffer it lands in is the one the
-                        // scores of half it + 2 wait for.  Each commit releases its
-                        // inputs as early as possible: the score buffer (through the
-                        // drain) after dQ^T, dS^T after dK, P^T and the Q/dO stage
-                        // after dV.
+                        // scores of half it + 2 wait for; dV next: the single P^T
+                        // tile it frees is the next thing the P/dS warps wait for.
+                        // Each commit releases its inputs as early as possible: the
+                        // score buffer (through the drain) after dQ^T, P^T after dV,
+                        // dS^T and the Q/dO stage after dK.
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
@@ -368,16 +369,16 @@ __global__ void __launch_bounds__(736, 1)
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
+                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
                                        (it > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[BB_DSE0 + pb]);
+                        tc_commit(&bars[BB_PE]);
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
                                        (it > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[BB_PE]);
+                        tc_commit(&bars[BB_DSE0 + pb]);
                         tc_commit(&bars[BB_QE0 + st]);
                     }
                 }
