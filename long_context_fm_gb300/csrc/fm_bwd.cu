@@ -128,15 +128,15 @@ struct BwdSmem {
     static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
     static constexpr int kStat = kList + kListCap * 4;      // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
-    static constexpr int kNumBar = 21;
+    static constexpr int kNumBar = 23;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
 };
 
 enum {
-    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_PF0, BB_PF1, BB_PE, BB_DSE0,
-    BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1
+    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_DF0, BB_DF1, BB_PF0, BB_PF1,
+    BB_PE, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1
 };
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
@@ -201,7 +201,9 @@ __global__ void __launch_bounds__(736, 1)
         }
         mbar_init(&bars[BB_SF0], 1);
         mbar_init(&bars[BB_SF1], 1);
-        mbar_init(&bars[BB_PF0], 512);    // four P/dS warpgroups
+        mbar_init(&bars[BB_DF0], 512);    // four P/dS warpgroups: dS^T written
+        mbar_init(&bars[BB_DF1], 512);
+        mbar_init(&bars[BB_PF0], 512);    // P^T written
         mbar_init(&bars[BB_PF1], 512);
         mbar_init(&bars[BB_PE], 1);
         mbar_init(&bars[BB_DSE0], 1);
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(736, 1)
                         tc_commit(&bars[BB_QE0 + st]);
                     } else {
                         const int qb = it & 1;         // score buffer: dQ^T goes into its S^T columns
-                        if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status)) {
+                        if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status)) {
                             ok = false;
                             break;
                         }
@@ -365,6 +367,11 @@ __global__ void __launch_bounds__(736, 1)
                                 mma_ss(tS0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048), idQ,
                                        (part > 0 || kk > 0));
                         tc_commit(&bars[BB_DQF0 + qb]);
+                        if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
 #pragma unroll
                         for (int part = 0; part < NPART; ++part)
 #pragma unroll
@@ -453,40 +460,48 @@ __global__ void __launch_bounds__(736, 1)
                     const uint64_t t2 = f2_sub(f2_pack(__uint_as_float(draw[c]), __uint_as_float(draw[c + 1])), dd2[c / 2]);
                     f2_unpack(f2_mul(f2_pack(p0, p1), t2), ds[c], ds[c + 1]);
                 }
-                // P^T is free once dV of the previous half has read it; this
-                // half's dS^T buffer once dK, dQ^T of the half that last used
-                // it have completed.
+                // dS^T first (its buffer is free once dK, dQ^T of the half that
+                // last used it have completed, normally long ago), announced on
+                // DF so that dQ^T can start; then P^T, whose single tile is free
+                // once dV of the previous half has read it, announced on PF.
                 const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;
                 const int back = S::kdSBufs;                 // halves between two uses of a dS^T buffer
-                if ((it >= 1 && !warp_wait(&bars[BB_PE], (it - 1) & 1, abort, a.status)) ||
-                    (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status))) { ok = false; break; }
-                uint8_t *bP = sP, *bdS = sdS + pb * S::kOp;
+                if (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status)) { ok = false; break; }
+                uint8_t *bdS = sdS + pb * S::kOp;
                 // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
 #pragma unroll
                 for (int u = 0; u < CW / 8; ++u) {
                     const int chunk = (c0 >> 3) + u;
                     const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
-                    uint32_t ph[4], pl[4], dh[4], dl[4];
+                    uint32_t dh[4], dl[4];
 #pragma unroll
                     for (int w2 = 0; w2 < 4; ++w2) {
                         const int c = 8 * u + 2 * w2;
-                        if (PRECISE) {
-                            split_bf16x2(p[c], p[c + 1], ph[w2], pl[w2]);
-                            split_bf16x2(ds[c], ds[c + 1], dh[w2], dl[w2]);
-                        } else {
-                            ph[w2] = pack_bf16x2(p[c], p[c + 1]);
-                            dh[w2] = pack_bf16x2(ds[c], ds[c + 1]);
-                        }
+                        if (PRECISE) split_bf16x2(ds[c], ds[c + 1], dh[w2], dl[w2]);
+                        else dh[w2] = pack_bf16x2(ds[c], ds[c + 1]);
                     }
-                    *reinterpret_cast<uint4 *>(bP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
                     *reinterpret_cast<uint4 *>(bdS + off) = make_uint4(dh[0], dh[1], dh[2], dh[3]);
-                    if (PRECISE) {
-                        *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-                        *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
-                    }
+                    if (PRECISE) *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();                  // S^T, dP^T reads of this half precede the dQ^T MMA
+                mbar_arrive(&bars[BB_DF0 + b]);
+                if (it >= 1 && !warp_wait(&bars[BB_PE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
+#pragma unroll
+                for (int u = 0; u < CW / 8; ++u) {
+                    const int chunk = (c0 >> 3) + u;
+                    const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
+                    uint32_t ph[4], pl[4];
+#pragma unroll
+                    for (int w2 = 0; w2 < 4; ++w2) {
+                        const int c = 8 * u + 2 * w2;
+                        if (PRECISE) split_bf16x2(p[c], p[c + 1], ph[w2], pl[w2]);
+                        else ph[w2] = pack_bf16x2(p[c], p[c + 1]);
+                    }
+                    *reinterpret_cast<uint4 *>(sP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                    if (PRECISE) *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                }
+                fence_proxy_async_smem();
                 mbar_arrive(&bars[BB_PF0 + b]);
             }
             // ------------------------------------------------ dK, dV epilogue
