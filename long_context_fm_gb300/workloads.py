@@ -14,7 +14,11 @@ written in canonical form: lower ``(N, N)``, upper ``(0, 0)``.
 The row form of the blog post "FlashMask技术" (§2.1 causal example, §3.3
 document-packing example) is an inclusive attend interval
 ``[col_start_i, col_end_i]`` per query row.  Workloads whose mask has such a
-form also return it, so the host converter can be checked against it.
+form also return it, so the host converter can be checked against it.  The
+multi-interval form (same blog, §6.1 item 1) gives each row K inclusive
+intervals; the window with sink tokens of the §5 streaming example (row i
+attends the first ``sink`` keys and the last ``window`` keys up to i) needs
+K = 2.
 
 Value recipe: fp32 N(0, 1) from ``torch.Generator`` seeded with ``seed`` in
 the order Q, K, V, dO, multiplied by ``input_scale`` and rounded to bf16
@@ -37,7 +41,8 @@ class Workload:
     H: int
     N: int
     d: int
-    mask: str                 # causal | docs_uniform | docs_lognormal | window | prefix | prefix_random | random_cols | full | none_attended
+    mask: str                 # causal | docs_uniform | docs_lognormal | window | window_sink | prefix
+                              # | prefix_random | random_cols | full | none_attended
     Hm: int = 1               # mask heads: 1 (shared) or H (per head)
     input_scale: float = 1.0
     params: dict = field(default_factory=dict)
@@ -67,6 +72,10 @@ FULL = {
     "long_packing_128k": Workload("long_packing_128k", B=1, H=8, N=131072, d=128,
                                   mask="docs_lognormal",
                                   params=dict(median=4096, sigma=1.0, lo=256, hi=32768)),
+    # The streaming-inference window (1024 keys) with 10 sink tokens, at the
+    # sliding-window workload's sizes.
+    "sliding_window_sink": Workload("sliding_window_sink", B=1, H=16, N=32768, d=128,
+                                    mask="window_sink", params=dict(window=1024, sink=10)),
 }
 
 # Small cases the oracle finishes in seconds: several tiles and a ragged tail.
@@ -88,6 +97,10 @@ SMALL = {
     "lognormal_small": Workload("lognormal_small", B=1, H=2, N=2048, d=128,
                                 mask="docs_lognormal",
                                 params=dict(median=200, sigma=1.0, lo=20, hi=900)),
+    "window_sink_small": Workload("window_sink_small", B=1, H=2, N=777, d=128, mask="window_sink",
+                                 params=dict(window=100, sink=10)),
+    "window_sink_d64": Workload("window_sink_d64", B=1, H=3, N=650, d=64, mask="window_sink",
+                                params=dict(window=200, sink=150)),
     "unmasked_small": Workload("unmasked_small", B=1, H=2, N=256, d=128, mask="full"),
     "all_masked_small": Workload("all_masked_small", B=1, H=1, N=200, d=64, mask="none_attended"),
 }
@@ -139,11 +152,14 @@ def _empty_bounds(N):
 
 
 def _one_mask(wl: Workload, b: int, hm: int, docs, rng):
-    """Column bounds (and row form when the mask has one) of one (batch, mask head)."""
+    """Column bounds, the one-interval row form when the mask has one, and
+    the K-interval row form ``(starts, ends)`` [N, K] when only that exists,
+    of one (batch, mask head)."""
     N = wl.N
     j = np.arange(N, dtype=np.int64)
     lts, lte, uts, ute = _empty_bounds(N)
     cs = ce = None
+    multi = None
     if wl.mask == "causal":
         ute[:] = j                                          # rows i < j masked
         cs = np.zeros(N, np.int32)
@@ -172,6 +188,17 @@ def _one_mask(wl: Workload, b: int, hm: int, docs, rng):
         lts[empty] = N
         cs = np.maximum(0, j - (W - 1)).astype(np.int32)
         ce = j.astype(np.int32)
+    elif wl.mask == "window_sink":
+        W, S = wl.params["window"], wl.params["sink"]
+        ute[:] = j                                          # causal: rows i < j
+        lo = np.minimum(j + W, N)                           # past the window ...
+        lts[:] = np.where(j < S, N, lo)                     # ... except sink columns
+        lte[:] = N
+        empty = lts >= lte
+        lts[empty] = N
+        starts = np.stack([np.zeros(N, np.int64), np.maximum(0, j - (W - 1))], axis=1)
+        ends = np.stack([np.minimum(S - 1, j), j], axis=1)
+        multi = (starts.astype(np.int32), ends.astype(np.int32))
     elif wl.mask in ("prefix", "prefix_random"):
         P = wl.params["prefix"]
         ute[P:] = j[P:]
@@ -208,27 +235,39 @@ def _one_mask(wl: Workload, b: int, hm: int, docs, rng):
         ce = np.zeros(N, np.int32)
     else:
         raise ValueError(wl.mask)
-    return (lts, lte, uts, ute), (None if cs is None else (cs, ce))
+    if cs is not None:
+        multi = (cs[:, None], ce[:, None])
+    return (lts, lte, uts, ute), (None if cs is None else (cs, ce)), multi
 
 
 def make_mask(wl: Workload, seed: int = 0):
-    """Column bounds ``lts, lte, uts, ute`` as int32 ``[B, Hm, N]`` plus the row
-    form ``(cs, ce)`` as int32 ``[B, Hm, N]`` or ``None``."""
+    """Column bounds ``lts, lte, uts, ute`` as int32 ``[B, Hm, N]``, the row
+    form ``rows = (cs, ce)`` as int32 ``[B, Hm, N]`` or ``None``, and the
+    K-interval row form ``row_intervals = (starts, ends)`` as int32
+    ``[B, Hm, N, K]`` or ``None`` (K = 1 wherever ``rows`` exists)."""
     docs = doc_lengths(wl, seed) if wl.mask.startswith("docs") else None
     rng = np.random.default_rng(seed)
     cols = np.empty((4, wl.B, wl.Hm, wl.N), np.int32)
     rows = np.empty((2, wl.B, wl.Hm, wl.N), np.int32)
-    has_rows = True
+    multi = None
+    has_rows = has_multi = True
     for b in range(wl.B):
         for hm in range(wl.Hm):
-            c, r = _one_mask(wl, b, hm, docs, rng)
+            c, r, mi = _one_mask(wl, b, hm, docs, rng)
             cols[:, b, hm] = np.stack(c)
             if r is None:
                 has_rows = False
             else:
                 rows[:, b, hm] = np.stack(r)
+            if mi is None:
+                has_multi = False
+            else:
+                if multi is None:
+                    multi = np.empty((2, wl.B, wl.Hm) + mi[0].shape, np.int32)
+                multi[:, b, hm] = np.stack(mi)
     return dict(lts=cols[0], lte=cols[1], uts=cols[2], ute=cols[3],
-                rows=(rows[0], rows[1]) if has_rows else None, docs=docs)
+                rows=(rows[0], rows[1]) if has_rows else None,
+                row_intervals=(multi[0], multi[1]) if has_multi else None, docs=docs)
 
 
 def make_inputs(wl: Workload, seed: int = 0, device="cpu", need_do: bool = True):

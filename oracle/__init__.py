@@ -52,6 +52,7 @@ def _configure(lib):
     I64 = ctypes.c_int64
     lib.oracle_dense_from_cols.argtypes = [P, P, P, P, I64, P]
     lib.oracle_dense_from_rows.argtypes = [P, P, I64, P]
+    lib.oracle_dense_from_row_intervals.argtypes = [P, P, I64, I64, P]
     lib.oracle_attended_pairs.argtypes = [P, P, P, P, I64]
     lib.oracle_attended_pairs.restype = I64
     lib.oracle_fwd_rows.argtypes = [P, P, P, P, P, P, P, I64, ctypes.c_int, ctypes.c_double,
@@ -106,6 +107,16 @@ def dense_from_rows(cs, ce) -> np.ndarray:
     N = cs.shape[0]
     M = np.empty((N, N), np.uint8)
     _load().oracle_dense_from_rows(_p(cs), _p(ce), N, _p(M))
+    return M.astype(bool)
+
+
+def dense_from_row_intervals(starts, ends) -> np.ndarray:
+    """Dense boolean mask (True = masked) of one head from K inclusive
+    intervals per row (int32 [N, K])."""
+    starts, ends = _i32(starts), _i32(ends)
+    N, K = starts.shape
+    M = np.empty((N, N), np.uint8)
+    _load().oracle_dense_from_row_intervals(_p(starts), _p(ends), N, K, _p(M))
     return M.astype(bool)
 
 

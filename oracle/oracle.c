@@ -17,6 +17,10 @@
  * Row form (blog post "FlashMask技术", §2.1 causal example, §3.3 document
  * packing, §4.1 item 3 "mask fused into the softmax"): row i attends column j
  * exactly when col_start_i <= j <= col_end_i.
+ * Multi-interval row form (same blog, §6.1 item 1, several disjoint intervals
+ * per row; the sink-token window of the §5 streaming example is one): row i
+ * attends column j exactly when start_ik <= j <= end_ik for some slot k
+ * (inclusive, as in §3.3; a slot with start > end attends nothing).
  *
  * Attention: the pages state the method is exact ("mathematically
  * equivalent", blog §2.2; "without sacrificing computational accuracy",
@@ -83,6 +87,20 @@ void oracle_dense_from_rows(const int32_t *cs, const int32_t *ce, int64_t N, uin
     for (int64_t i = 0; i < N; ++i)
         for (int64_t j = 0; j < N; ++j)
             M[i * N + j] = (uint8_t)!(cs[i] <= j && j <= ce[i]);
+}
+
+/* M[i*N + j] = 1 where no interval of row i contains j (starts, ends: [N, K]). */
+void oracle_dense_from_row_intervals(const int32_t *starts, const int32_t *ends, int64_t N, int64_t K,
+                                     uint8_t *M)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < N; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            int attended = 0;
+            for (int64_t k = 0; k < K; ++k)
+                if (starts[i * K + k] <= j && j <= ends[i * K + k]) attended = 1;
+            M[i * N + j] = (uint8_t)!attended;
+        }
 }
 
 /* Number of attended (unmasked) pairs, counted element by element. */

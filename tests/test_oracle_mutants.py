@@ -26,6 +26,12 @@ MUTANTS = {
     "dV missing P": ("dv[c] += p * (double)dO[i * d + c];", "dv[c] += (double)dO[i * d + c];"),
     "label uses min for max": ("(L0max <= qb && L1min >= qe)", "(L0min <= qb && L1min >= qe)"),
     "full test uses max": ("(U0min >= qe || U1max <= qb)", "(U0max >= qe || U1max <= qb)"),
+    "interval end exclusive": ("if (starts[i * K + k] <= j && j <= ends[i * K + k]) attended = 1;",
+                               "if (starts[i * K + k] <= j && j < ends[i * K + k]) attended = 1;"),
+    "only the first interval": ("for (int64_t k = 0; k < K; ++k)\n                if (starts",
+                                "for (int64_t k = 0; k < 1; ++k)\n                if (starts"),
+    "last interval wins": ("if (starts[i * K + k] <= j && j <= ends[i * K + k]) attended = 1;",
+                           "attended = (starts[i * K + k] <= j && j <= ends[i * K + k]);"),
 }
 
 PINS = [
@@ -36,6 +42,10 @@ PINS = [
     pins.test_row_and_column_forms_give_the_same_dense_mask,
     pins.test_golden_causal_example,
     pins.test_golden_doc_packing_example,
+    pins.test_golden_multi_interval_example,
+    pins.test_multi_interval_reduces_to_one_interval_rows,
+    pins.test_multi_interval_union_invariants,
+    pins.test_window_sink_row_and_column_forms_agree,
     lambda: [pins.test_labels_equal_exact_on_structured_masks(n, 128, 128) for n in
              ("causal_ragged", "docs_small", "window_small", "prefix_small")],
     lambda: [pins.test_labels_sound_on_arbitrary_bounds(s) for s in range(6)],

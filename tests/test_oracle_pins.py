@@ -6,8 +6,8 @@
   fully masked rows, D = dO.O, invariance of O and dQ under a shift of every key);
 - closed forms: attended-pair counts and the tile counts of causal masks
   ("about half of the GEMMs skipped", blog "FlashMask技术" §1 item 2 and §2.2);
-- the pages' worked examples (blog §2.1 causal row form, §3.3 document packing)
-  stored under tests/golden/.
+- the pages' worked examples (blog §2.1 causal row form, §3.3 document packing,
+  §6.1 multi-interval rows) stored under tests/golden/.
 """
 import json
 import os
@@ -175,6 +175,99 @@ def test_row_and_column_forms_give_the_same_dense_mask():
                 assert np.array_equal(Mr, Mc), (wl.name, b, hm)
 
 
+def _multi_from_golden(gd):
+    N = gd["N"]
+    K = max(len(v) for v in gd["rows"].values())
+    starts = np.ones((N, K), np.int32)          # unused slots: start > end
+    ends = np.zeros((N, K), np.int32)
+    for r, ivs in gd["rows"].items():
+        for k, (a, b) in enumerate(ivs):
+            starts[int(r), k], ends[int(r), k] = a, b
+    return starts, ends
+
+
+def test_golden_multi_interval_example():
+    """Blog §6.1 item 1: the printed two-row example, hand-derived counts and columns."""
+    gd = json.load(open(os.path.join(GOLDEN, "multi_interval_example.json")))
+    N = gd["N"]
+    starts, ends = _multi_from_golden(gd)
+    M = oracle.dense_from_row_intervals(starts, ends)
+    for r, n in gd["attended_per_row"].items():
+        assert int((~M[int(r)]).sum()) == n
+    assert int((~M).sum()) == gd["attended_pairs"]
+    assert np.array_equal(np.flatnonzero(~M[0]), np.r_[0:101, 200:301])
+    # the hand-written column spot values describe the same mask
+    for j, (a, b, c, d) in gd["expect_columns"].items():
+        col = np.zeros(N, bool)
+        col[a:b] = True
+        col[c:d] = True
+        assert np.array_equal(M[:, int(j)], col), j
+
+
+def test_multi_interval_reduces_to_one_interval_rows():
+    """K = 1 is the one-interval row rule; extra unused slots change nothing."""
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        N = int(rng.integers(1, 60))
+        cs = rng.integers(0, N, size=N).astype(np.int32)
+        ce = (cs + rng.integers(-3, N, size=N)).clip(max=N - 1).astype(np.int32)
+        Mr = oracle.dense_from_rows(cs, ce)
+        assert np.array_equal(oracle.dense_from_row_intervals(cs[:, None], ce[:, None]), Mr)
+        pad_s = np.concatenate([cs[:, None], np.full((N, 2), 7, np.int32)], axis=1)
+        pad_e = np.concatenate([ce[:, None], np.full((N, 2), 3, np.int32)], axis=1)
+        assert np.array_equal(oracle.dense_from_row_intervals(pad_s, pad_e), Mr)
+
+
+def test_multi_interval_union_invariants():
+    """The attended set is the union of the slots: slot order does not matter, an
+    interval split into two touching pieces or covered by an overlapping one
+    changes nothing, and counts equal the size of the union."""
+    rng = np.random.default_rng(6)
+    for _ in range(20):
+        N = int(rng.integers(2, 50))
+        K = int(rng.integers(1, 5))
+        a = rng.integers(0, N, size=(N, K)); b = rng.integers(0, N, size=(N, K))
+        s, e = np.minimum(a, b).astype(np.int32), np.maximum(a, b).astype(np.int32)
+        M = oracle.dense_from_row_intervals(s, e)
+        perm = rng.permutation(K)
+        assert np.array_equal(oracle.dense_from_row_intervals(s[:, perm], e[:, perm]), M)
+        mid = (s[:, :1] + e[:, :1]) // 2                                  # slot 0 -> [s, mid], [mid + 1, e]
+        s2 = np.concatenate([s, mid + 1], axis=1).astype(np.int32)
+        e2 = np.concatenate([mid, e[:, 1:], e[:, :1]], axis=1).astype(np.int32)
+        assert np.array_equal(oracle.dense_from_row_intervals(s2, e2), M)
+        s3 = np.concatenate([s, s[:, :1]], axis=1).astype(np.int32)      # slot 0 repeated
+        e3 = np.concatenate([e, e[:, :1]], axis=1).astype(np.int32)
+        assert np.array_equal(oracle.dense_from_row_intervals(s3, e3), M)
+        for i in range(N):
+            want = set()
+            for k in range(K):
+                want |= set(range(s[i, k], e[i, k] + 1))
+            assert int((~M[i]).sum()) == len(want)
+
+
+def test_window_sink_row_and_column_forms_agree():
+    for name in ("window_sink_small", "window_sink_d64"):
+        wl = W.SMALL[name]
+        m = _mask_np(wl)
+        assert m["rows"] is None and m["row_intervals"][0].shape == (1, 1, wl.N, 2)
+        Mi = oracle.dense_from_row_intervals(m["row_intervals"][0][0, 0], m["row_intervals"][1][0, 0])
+        assert np.array_equal(Mi, oracle.dense_from_cols(*_bounds(m)))
+
+
+@pytest.mark.parametrize("name", ["window_sink_small", "window_sink_d64", "sliding_window_sink"])
+def test_window_sink_attended_pairs_closed_form(name):
+    """Row i attends min(i + 1, W) window keys plus the sink keys left of its
+    window: max(0, min(S, i - W + 1))."""
+    wl = W.SMALL.get(name) or W.FULL[name]
+    Wn, S, N = wl.params["window"], wl.params["sink"], wl.N
+    i = np.arange(N, dtype=np.int64)
+    want = int((np.minimum(i + 1, Wn) + np.maximum(0, np.minimum(S, i - Wn + 1))).sum())
+    if name == "sliding_window_sink":
+        assert want == 33030656 + 10 * (N - 1033) + 45
+    m = _mask_np(wl)
+    assert oracle.attended_pairs(*_bounds(m)) == want
+
+
 def _counts(lbl):
     return dict(skip=int((lbl == 0).sum()), full=int((lbl == 1).sum()), partial=int((lbl == 2).sum()))
 
@@ -253,7 +346,8 @@ def test_attended_pairs_docs_closed_form():
 
 @pytest.mark.parametrize("name", ["tiny_causal", "doc_packing", "sliding_window", "prefix_lm",
                                   "causal_ragged", "docs_small", "window_small", "prefix_small",
-                                  "lognormal_small", "unmasked_small", "all_masked_small"])
+                                  "lognormal_small", "unmasked_small", "all_masked_small",
+                                  "window_sink_small", "window_sink_d64", "sliding_window_sink"])
 @pytest.mark.parametrize("bq,bk", [(128, 128), (64, 128), (64, 64), (128, 64)])
 def test_labels_equal_exact_on_structured_masks(name, bq, bk):
     wl = W.FULL.get(name) or W.SMALL[name]
