@@ -215,9 +215,13 @@ def run_fm(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * hb[0].numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
 
+    multi = m["row_intervals"]
+
     def e2e_step():
         if rows is not None:                                     # host conversion of the row form
             cols = fm.fm_mask_from_rows(*rows)
+        elif multi is not None:                                  # several intervals per row
+            cols = fm.fm_mask_from_row_intervals(*multi)
         else:
             cols = [m[x] for x in ("lts", "lte", "uts", "ute")]
         for dst, src in zip(hb, cols):
@@ -243,6 +247,28 @@ def run_fm(args, rank, world, local_rank):
     ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
                 avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h)
+
+
+def mask_description(wl):
+    p = wl.params
+    return {
+        "causal": "causal",
+        "docs_uniform": f"documents of uniform length in [{p.get('lo')}, {p.get('hi')}], causal within document",
+        "docs_lognormal": (f"log-normal documents (median {p.get('median')}, sigma {p.get('sigma')}, "
+                           f"clip [{p.get('lo')}, {p.get('hi')}]), causal within document"),
+        "window": f"causal sliding window of {p.get('window')} keys",
+        "window_sink": f"causal sliding window of {p.get('window')} keys plus {p.get('sink')} sink keys",
+        "prefix": f"prefix LM: bidirectional prefix of {p.get('prefix')}, causal after it",
+        "prefix_random": (f"prefix of {p.get('prefix')} plus a random lower masked range per column "
+                          "(lts uniform in [j, N])"),
+    }.get(wl.mask, wl.mask)
+
+
+def l2_note(wl):
+    gib = 4 * wl.B * wl.H * wl.N * wl.d * 2 / 2 ** 30
+    if gib * 2 ** 30 > 129e6:
+        return f"inputs larger than L2 (Q, K, V, dO {gib:.2f} GiB), no flush"
+    return f"inputs of {gib * 1024:.0f} MiB (Q, K, V, dO) may stay in the 129 MB L2: no flush"
 
 
 def cpu_baseline_sample(wl, m, max_docs=3, rows=4096):
@@ -333,10 +359,10 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": r["wl"].name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
-                       "mask": "log-normal documents (median 4096, sigma 1, clip [256, 32768]), causal within document",
+                       "mask": mask_description(wl),
                        "attended_pairs": r["pairs"], "outputs": "fp32 O, dQ, dK, dV",
                        "precision": "standard (bf16 P and dS tensor-core operands, fp32 accumulation)",
-                       "l2": "inputs larger than L2 (Q, K, V, dO 1 GiB), no flush"},
+                       "l2": l2_note(wl)},
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
             "frac_of_peak": {"fwd": fwd_tflops / peak_burst, "fwd_bwd": value / world / peak_sus,
                              "peaks": f"{src}: bf16 burst {peak_burst}, sustained {peak_sus}"},

@@ -106,10 +106,33 @@ FM_API fm_status fm_mask_from_rows(const int32_t *cs, const int32_t *ce, int B, 
                             int32_t *lts, int32_t *lte, int32_t *uts, int32_t *ute);
 
 /*
+ * fm_mask_from_row_intervals — HOST, synchronous.
+ * Passage: blog "FlashMask技术" §6.1 item 1 (multi-interval extension:
+ * several disjoint attend intervals per row, printed as row 0 -> (0, 100),
+ * (200, 300) and row 1 -> (0, 50), (150, 250)), read with the inclusive
+ * interval convention of §3.3.  The window-with-sink-tokens mask of the §5
+ * streaming-inference example (row i attends [0, sink) and (i - window, i])
+ * is such a two-interval row form.
+ * starts, ends: host int32 [B, Hm, N, K], K >= 1 interval slots per row;
+ * slot (s, e) with s > e is unused; otherwise 0 <= s <= e < N is required
+ * (else FM_ERR_BAD_BOUNDS).  Row i attends the union of its intervals, which
+ * may overlap, touch or come in any order.  Output and errors as for
+ * fm_mask_from_rows (which is the K = 1 case, with identical results): each
+ * column's non-attending rows must form at most two ranges, else
+ * FM_ERR_UNREPRESENTABLE.  Runs in O(N K log K) per (b, hm).
+ */
+FM_API fm_status fm_mask_from_row_intervals(const int32_t *starts, const int32_t *ends, int K, int B,
+                                     int Hm, int N, int32_t *lts, int32_t *lte, int32_t *uts,
+                                     int32_t *ute);
+
+/*
  * Plan = tile labels plus, per Q tile, the ordered list of non-skip KV tiles
  * and, per KV tile, the list of non-skip Q tiles (blog §4.1 item 2: decide
- * before a KV block is loaded whether it is needed at all).  Opaque device
- * buffer of fm_plan_bytes() bytes, 256-byte aligned, written by
+ * before a KV block is loaded whether it is needed at all), plus the order in
+ * which the attention kernels take their tiles: longest list first, in
+ * half-octave length buckets, so that a tile with a long list (sink columns,
+ * the first tiles of a long document) starts in the first wave.  Opaque
+ * device buffer of fm_plan_bytes() bytes, 256-byte aligned, written by
  * fm_tile_classify and read by fm_attn_fwd / fm_attn_bwd.
  * bq, bk in {64, 128}; the attention kernels need bq = bk = 128.
  * Returns 0 for invalid sizes.
@@ -127,7 +150,8 @@ FM_API size_t fm_plan_bytes(int B, int Hm, int N, int bq, int bk);
  *   PARTIAL otherwise (tile ends clipped to N).
  * labels (nullable): device uint8 [B, Hm, n_q, n_k] copy of the labels.
  * dev_status: device int32 (required).  Bounds outside [0, N] set
- * FM_ERR_BAD_BOUNDS there.
+ * FM_ERR_BAD_BOUNDS there.  Three launches on the stream: per-tile bound
+ * min/max, labels and lists, work order.
  */
 FM_API fm_status fm_tile_classify(fm_bounds m, int bq, int bk, void *plan, size_t plan_bytes,
                            uint8_t *labels, int32_t *dev_status, fm_stream_t stream);
@@ -210,7 +234,7 @@ FM_API fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const void *v
  * stops recording.  Returns the number of records written, or -1 on error.
  */
 enum { FM_K_CLASSIFY_MINMAX = 0, FM_K_CLASSIFY_LISTS = 1, FM_K_FWD = 2, FM_K_BWD_PRE = 3,
-       FM_K_BWD = 4, FM_K_BWD_POST = 5, FM_K_COUNT = 6 };
+       FM_K_BWD = 4, FM_K_BWD_POST = 5, FM_K_CLASSIFY_ORDER = 6, FM_K_COUNT = 7 };
 typedef struct {
     int32_t kernel;
     float ms;

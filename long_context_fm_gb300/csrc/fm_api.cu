@@ -30,7 +30,7 @@ fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 
 bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
 

@@ -176,46 +176,55 @@ __global__ void __launch_bounds__(736, 1)
     int *cnt_sh = reinterpret_cast<int *>(smem + S::kMisc + 8);
     int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
 
+    int *unit_sh = reinterpret_cast<int *>(smem + S::kMisc + 16);   // KV tile, head, batch
+
     const int warp = warp_id(), lane = lane_id();
     const PlanLayout &L = a.L;
-    const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
-    const int bh = b * a.H + h;
     const int N = a.N;
-    const int kb = kt * 128;
 
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
         const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(a.plan);
-        const bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
-                        ph->bq == 128 && ph->bk == 128;
-        if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
-        const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
-        if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
-        *ok_sh = ok && aligned;
-        *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)sidx * L.n_k + kt] : 0;
-        *abort = 0;
-        mbar_init(&bars[BB_KV], 1);
-        for (int s2 = 0; s2 < NST; ++s2) {
-            mbar_init(&bars[BB_QF0 + s2], 33);
-            mbar_init(&bars[BB_QE0 + s2], 2);     // scores and gradients issuers
+        bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
+                  ph->bq == 128 && ph->bk == 128;
+        // KV tiles longest column list first (the plan's bucketed order); ok is warp-uniform.
+        int ut = 0, uh = 0, ub = 0;
+        const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+        if (ok)
+            ok = plan_unit(reinterpret_cast<const int32_t *>(a.plan + L.off_col_order),
+                           reinterpret_cast<const int32_t *>(a.plan + L.off_col_bstart), L.n_k, a.B, a.Hm, a.H, cta,
+                           &ut, &uh, &ub);
+        if (lane == 0) {
+            if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
+            const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
+            if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
+            *ok_sh = ok && aligned;
+            unit_sh[0] = ut; unit_sh[1] = uh; unit_sh[2] = ub;
+            const int us = ub * a.Hm + (a.Hm == 1 ? 0 : uh);
+            *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)us * L.n_k + ut] : 0;
+            *abort = 0;
+            mbar_init(&bars[BB_KV], 1);
+            for (int s2 = 0; s2 < NST; ++s2) {
+                mbar_init(&bars[BB_QF0 + s2], 33);
+                mbar_init(&bars[BB_QE0 + s2], 2);     // scores and gradients issuers
+            }
+            mbar_init(&bars[BB_SF0], 1);
+            mbar_init(&bars[BB_SF1], 1);
+            mbar_init(&bars[BB_DF0], 512);    // four P/dS warpgroups: dS^T written
+            mbar_init(&bars[BB_DF1], 512);
+            mbar_init(&bars[BB_PF0], 512);    // P^T written
+            mbar_init(&bars[BB_PF1], 512);
+            mbar_init(&bars[BB_PE], 1);
+            mbar_init(&bars[BB_DSE0], 1);
+            mbar_init(&bars[BB_DSE1], 1);
+            mbar_init(&bars[BB_DQF0], 1);
+            mbar_init(&bars[BB_DQF1], 1);
+            mbar_init(&bars[BB_DQE0], 128);
+            mbar_init(&bars[BB_DQE1], 128);
+            mbar_init(&bars[BB_ACC], 1);
+            mbar_init(&bars[BB_DRAIN0], 1);
+            mbar_init(&bars[BB_DRAIN1], 1);
+            fence_barrier_init();
         }
-        mbar_init(&bars[BB_SF0], 1);
-        mbar_init(&bars[BB_SF1], 1);
-        mbar_init(&bars[BB_DF0], 512);    // four P/dS warpgroups: dS^T written
-        mbar_init(&bars[BB_DF1], 512);
-        mbar_init(&bars[BB_PF0], 512);    // P^T written
-        mbar_init(&bars[BB_PF1], 512);
-        mbar_init(&bars[BB_PE], 1);
-        mbar_init(&bars[BB_DSE0], 1);
-        mbar_init(&bars[BB_DSE1], 1);
-        mbar_init(&bars[BB_DQF0], 1);
-        mbar_init(&bars[BB_DQF1], 1);
-        mbar_init(&bars[BB_DQE0], 128);
-        mbar_init(&bars[BB_DQE1], 128);
-        mbar_init(&bars[BB_ACC], 1);
-        mbar_init(&bars[BB_DRAIN0], 1);
-        mbar_init(&bars[BB_DRAIN1], 1);
-        fence_barrier_init();
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
@@ -225,6 +234,10 @@ __global__ void __launch_bounds__(736, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    const int kt = unit_sh[0], h = unit_sh[1], b = unit_sh[2];
+    const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
+    const int bh = b * a.H + h;
+    const int kb = kt * 128;
     // TMEM: dK, dV, S^T, dP^T, and dQ^T double-buffered (half it uses buffer it & 1).
     // Score buffer b = half & 1: S^T at 256 + 128 b, dP^T at 320 + 128 b; the
     // half's dQ^T reuses the S^T columns once P^T/dS^T have been written.

@@ -1,6 +1,6 @@
 // Tile classification (blog "FlashMask技术" §2.2: per (Q block, KV block)
 // skip / full GEMM / masked GEMM; §4.1 item 2: decide before a KV block is
-// loaded).  Two launches:
+// loaded).  Three launches:
 //   1. minmax: one CTA per (b*Hm, KV tile) reduces the tile's canonicalised
 //      column bounds to 8 int32 (min and max of each bound), validates the
 //      bounds and writes the plan header;
@@ -8,7 +8,12 @@
 //      the ordered list of its non-skip KV tiles; one CTA per (b*Hm, KV tile)
 //      writes the list of non-skip Q tiles of that KV tile (for the
 //      KV-major backward).  Labels are recomputed from the 8 numbers, so the
-//      two halves need no other dependency.
+//      two halves need no other dependency;
+//   3. order:  a stable counting sort of the list lengths, longest first, one
+//      CTA per direction; the attention kernels take their units in this
+//      order, so a tile with a long list (a sink column, a long document's
+//      last rows) starts in the first wave instead of wherever its index
+//      puts it.
 // HBM traffic: 16 bytes per column read, n_q*n_k label bytes and <= 8 bytes
 // per non-skip pair written.
 #include <cuda_runtime.h>
@@ -72,6 +77,8 @@ __global__ void __launch_bounds__(128) classify_minmax_kernel(fm_bounds m, PlanL
         PlanHeader *h = reinterpret_cast<PlanHeader *>(plan);
         h->B = L.B; h->Hm = L.Hm; h->N = L.N; h->bq = L.bq; h->bk = L.bk;
         h->n_q = L.n_q; h->n_k = L.n_k; h->total = L.total;
+        h->off_row_order = L.off_row_order; h->off_col_order = L.off_col_order;
+        h->off_row_bstart = L.off_row_bstart; h->off_col_bstart = L.off_col_bstart;
         __threadfence();
         h->magic = kPlanMagic;
     }
@@ -146,6 +153,58 @@ __global__ void __launch_bounds__(128) classify_lists_kernel(PlanLayout L, uint8
     if (threadIdx.x == 0) *cnt = base_sh;
 }
 
+constexpr int kOrderThreads = 1024;
+
+// blockIdx.x == 0: order of the B*Hm*n_q Q-tile entries by row-list length;
+// blockIdx.x == 1: order of the B*Hm*n_k KV-tile entries by column-list length.
+// A counting sort over the length buckets of order_bucket (longest first),
+// stable: inside a bucket entries keep their index order, so the plan is
+// deterministic.  Also writes the first entry of every bucket.
+__global__ void __launch_bounds__(kOrderThreads) classify_order_kernel(PlanLayout L, uint8_t *plan)
+{
+    const bool rows = blockIdx.x == 0;
+    const int64_t n_e = (int64_t)L.B * L.Hm * (rows ? L.n_q : L.n_k);
+    const int32_t *len = reinterpret_cast<const int32_t *>(plan + (rows ? L.off_row_cnt : L.off_col_cnt));
+    int32_t *order = reinterpret_cast<int32_t *>(plan + (rows ? L.off_row_order : L.off_col_order));
+    int32_t *bstart = reinterpret_cast<int32_t *>(plan + (rows ? L.off_row_bstart : L.off_col_bstart));
+
+    __shared__ int hist[kOrderBuckets];
+    __shared__ int next[kOrderBuckets];
+    const int t = threadIdx.x, w = t >> 5, ln = t & 31;
+    if (t < kOrderBuckets) hist[t] = 0;
+    __syncthreads();
+    for (int64_t e = t; e < n_e; e += kOrderThreads) atomicAdd(&hist[order_bucket(len[e])], 1);
+    __syncthreads();
+    if (t == 0) {
+        int run = 0;
+        for (int k = 0; k < kOrderBuckets; ++k) {
+            next[k] = run;
+            bstart[k] = run;
+            run += hist[k];
+        }
+        bstart[kOrderBuckets] = run;
+    }
+    __syncthreads();
+    // stable scatter: chunks in index order, the warps of a chunk one after another
+    for (int64_t c0 = 0; c0 < n_e; c0 += kOrderThreads) {
+        const int64_t e = c0 + t;
+        const int bk = e < n_e ? order_bucket(len[e]) : -1;
+        for (int ww = 0; ww < kOrderThreads / 32; ++ww) {
+            if (w == ww) {
+                const unsigned peers = __match_any_sync(0xffffffffu, bk);
+                const int rank = __popc(peers & ((1u << ln) - 1u));
+                const int base = bk >= 0 ? next[bk] : 0;
+                __syncwarp();
+                if (bk >= 0) {
+                    order[base + rank] = (int32_t)e;
+                    if (rank == 0) next[bk] = base + __popc(peers);
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 }  // namespace fm
 
 using namespace fm;
@@ -165,6 +224,11 @@ fm_status fm_classify_launch(fm_bounds m, int bq, int bk, void *plan, uint8_t *l
     {
         ProfScope ps(kKClassifyLists, stream);
         classify_lists_kernel<<<dim3(L.n_q + L.n_k, S), 128, 0, stream>>>(L, (uint8_t *)plan, labels);
+    }
+    if (cudaPeekAtLastError() != cudaSuccess) return FM_ERR_CUDA;
+    {
+        ProfScope ps(kKClassifyOrder, stream);
+        classify_order_kernel<<<2, kOrderThreads, 0, stream>>>(L, (uint8_t *)plan);
     }
     if (cudaPeekAtLastError() != cudaSuccess) return FM_ERR_CUDA;
     return FM_OK;

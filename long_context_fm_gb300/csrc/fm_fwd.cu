@@ -97,44 +97,52 @@ __global__ void __launch_bounds__(352, 1)
     int *cnt_sh = reinterpret_cast<int *>(smem + S::kMisc + 8);
     int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
 
+    int *unit_sh = reinterpret_cast<int *>(smem + S::kMisc + 16);   // Q tile, head, batch
+
     const int warp = warp_id(), lane = lane_id();
     const PlanLayout &L = a.L;
-    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;   // heavy causal tiles first
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
-    const int bh = b * a.H + h;
     const int N = a.N;
 
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
         const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(a.plan);
-        const bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
-                        ph->bq == 128 && ph->bk == 128;
-        if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
-        const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
-        if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
-        *ok_sh = ok && aligned;
-        const int32_t *rc = reinterpret_cast<const int32_t *>(a.plan + L.off_row_cnt) + (int64_t)sidx * L.n_q;
-        *cnt_sh = ok ? rc[qt] : 0;
-        *abort = 0;
-        mbar_init(&bars[FB_Q], 1);
-        for (int s = 0; s < KS; ++s) {
-            mbar_init(&bars[FB_KF0 + s], 1);
-            mbar_init(&bars[FB_KE0 + s], 1);
+        bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
+                  ph->bq == 128 && ph->bk == 128;
+        // Q tiles longest row list first (the plan's bucketed order); ok is warp-uniform.
+        int ut = 0, uh = 0, ub = 0;
+        const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+        if (ok)
+            ok = plan_unit(reinterpret_cast<const int32_t *>(a.plan + L.off_row_order),
+                           reinterpret_cast<const int32_t *>(a.plan + L.off_row_bstart), L.n_q, a.B, a.Hm, a.H, cta,
+                           &ut, &uh, &ub);
+        if (lane == 0) {
+            if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
+            const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
+            if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
+            *ok_sh = ok && aligned;
+            unit_sh[0] = ut; unit_sh[1] = uh; unit_sh[2] = ub;
+            const int us = ub * a.Hm + (a.Hm == 1 ? 0 : uh);
+            *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_row_cnt)[(int64_t)us * L.n_q + ut] : 0;
+            *abort = 0;
+            mbar_init(&bars[FB_Q], 1);
+            for (int s = 0; s < KS; ++s) {
+                mbar_init(&bars[FB_KF0 + s], 1);
+                mbar_init(&bars[FB_KE0 + s], 1);
+            }
+            for (int s = 0; s < VS; ++s) {
+                mbar_init(&bars[FB_VF0 + s], 1);
+                mbar_init(&bars[FB_VE0 + s], 1);
+                mbar_init(&bars[FB_BF0 + s], 32);
+            }
+            // One O barrier per score buffer: the PV of tile t commits to O_{t mod 3},
+            // so every wait below targets a barrier at most one phase behind.
+            for (int s = 0; s < kSB; ++s) {
+                mbar_init(&bars[FB_S0 + s], 1);
+                mbar_init(&bars[FB_P0 + s], 256);
+                mbar_init(&bars[FB_O0 + s], 1);
+            }
+            mbar_init(&bars[FB_DRAIN], 1);
+            fence_barrier_init();
         }
-        for (int s = 0; s < VS; ++s) {
-            mbar_init(&bars[FB_VF0 + s], 1);
-            mbar_init(&bars[FB_VE0 + s], 1);
-            mbar_init(&bars[FB_BF0 + s], 32);
-        }
-        // One O barrier per score buffer: the PV of tile t commits to O_{t mod 3},
-        // so every wait below targets a barrier at most one phase behind.
-        for (int s = 0; s < kSB; ++s) {
-            mbar_init(&bars[FB_S0 + s], 1);
-            mbar_init(&bars[FB_P0 + s], 256);
-            mbar_init(&bars[FB_O0 + s], 1);
-        }
-        mbar_init(&bars[FB_DRAIN], 1);
-        fence_barrier_init();
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, 512);
@@ -144,6 +152,9 @@ __global__ void __launch_bounds__(352, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    const int qt = unit_sh[0], h = unit_sh[1], b = unit_sh[2];
+    const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
+    const int bh = b * a.H + h;
     const int n = *cnt_sh;
     const int32_t *glist =
         reinterpret_cast<const int32_t *>(a.plan + L.off_row_list) + ((int64_t)sidx * L.n_q + qt) * L.n_k;

@@ -19,7 +19,8 @@ constexpr int kLabelShift = 28;               // list entry = tile | (label << 2
 constexpr int32_t kTileMask = (1 << kLabelShift) - 1;
 
 // Plan layout: header, per-KV-tile min/max, labels, per-Q-tile lists (CSR),
-// per-KV-tile lists (CSC).  Every section starts on a 256-byte boundary.
+// per-KV-tile lists (CSC), and the two work orders.  Every section starts on a
+// 256-byte boundary.
 struct PlanLayout {
     int32_t B, Hm, N, bq, bk, n_q, n_k;
     int64_t off_minmax;    // int32 [B*Hm][n_k][8]
@@ -28,16 +29,34 @@ struct PlanLayout {
     int64_t off_row_list;  // int32 [B*Hm][n_q][n_k]  kv tile | label << 28
     int64_t off_col_cnt;   // int32 [B*Hm][n_k]
     int64_t off_col_list;  // int32 [B*Hm][n_k][n_q]  q tile | label << 28
+    int64_t off_row_order; // int32 [B*Hm*n_q]  entries s*n_q + q tile, longest list first
+    int64_t off_col_order; // int32 [B*Hm*n_k]  entries s*n_k + kv tile, longest list first
+    int64_t off_row_bstart;// int32 [kOrderBuckets + 1]  first row-order entry of each bucket
+    int64_t off_col_bstart;// int32 [kOrderBuckets + 1]  first col-order entry of each bucket
     int64_t total;
 };
 
-struct PlanHeader {        // first 64 bytes of a plan, written by the classifier
+// Work-order buckets: list length len > 0 falls in half-octave 2*floor(log2 len)
+// + (second bit of len), len = 0 in the last bucket; bucket 0 holds the
+// longest lists.  Within a bucket entries keep their index order.
+constexpr int kOrderBuckets = 64;
+FM_HD int order_bucket(int len)
+{
+    if (len <= 0) return kOrderBuckets - 1;
+    int lg = 0;
+    while ((len >> lg) > 1) ++lg;
+    const int half = lg > 0 ? (len >> (lg - 1)) & 1 : 0;
+    return kOrderBuckets - 2 - (2 * lg + half);          // lg <= 30: result in [0, 62]
+}
+
+struct PlanHeader {        // first 128 bytes of a plan, written by the classifier
     uint32_t magic;
     int32_t B, Hm, N, bq, bk, n_q, n_k;
     int64_t total;
-    int32_t pad[6];
+    int64_t off_row_order, off_col_order, off_row_bstart, off_col_bstart;
+    int32_t pad[14];
 };
-static_assert(sizeof(PlanHeader) == 64, "plan header size");
+static_assert(sizeof(PlanHeader) == 128, "plan header size");
 
 FM_HD int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
@@ -48,6 +67,7 @@ FM_HD bool plan_layout(int B, int Hm, int N, int bq, int bk, PlanLayout *L)
     const int64_t n_q = (N + bq - 1) / bq, n_k = (N + bk - 1) / bk;
     if (n_q >= kTileMask || n_k >= kTileMask) return false;
     const int64_t S = (int64_t)B * Hm;
+    if (S * (n_q > n_k ? n_q : n_k) >= ((int64_t)1 << 31)) return false;   // order entries are int32
     L->B = B; L->Hm = Hm; L->N = N; L->bq = bq; L->bk = bk;
     L->n_q = (int32_t)n_q; L->n_k = (int32_t)n_k;
     int64_t off = 256;
@@ -57,9 +77,53 @@ FM_HD bool plan_layout(int B, int Hm, int N, int bq, int bk, PlanLayout *L)
     L->off_row_list = off; off = align256(off + S * n_q * n_k * 4);
     L->off_col_cnt = off;  off = align256(off + S * n_k * 4);
     L->off_col_list = off; off = align256(off + S * n_k * n_q * 4);
+    L->off_row_order = off; off = align256(off + S * n_q * 4);
+    L->off_col_order = off; off = align256(off + S * n_k * 4);
+    L->off_row_bstart = off; off = align256(off + (kOrderBuckets + 1) * 4);
+    L->off_col_bstart = off; off = align256(off + (kOrderBuckets + 1) * 4);
     L->total = off;
     return true;
 }
+
+#if defined(__CUDACC__)
+// Work unit of the attention CTA with linear block index c, for a grid of
+// n_tiles x H x B CTAs; called by all 32 lanes of one warp, result valid in
+// every lane.  Order entries (s * n_tiles + tile, s = b * Hm + hm) are grouped
+// into length buckets, longest first; one entry stands for the rep heads that
+// read mask head hm (rep = H for a shared mask, else 1).  Inside a bucket the
+// heads are outermost, so CTAs that run together mostly share a head and read
+// neighbouring tiles.  Returns false on a plan not written by the classifier.
+__device__ __forceinline__ bool plan_unit(const int32_t *order, const int32_t *bstart, int n_tiles, int B,
+                                          int Hm, int H, int64_t c, int *tile, int *h, int *b)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t rep = (Hm == 1) ? H : 1;
+    const int64_t n_e = (int64_t)B * Hm * n_tiles;
+    // bucket starts: lane l holds buckets l and l + 32, lane 0 also the end
+    const int64_t s0 = bstart[lane], s1 = bstart[lane + 32], s_end = bstart[kOrderBuckets];
+    if (__any_sync(0xffffffffu, s0 < 0 || s0 > n_e || s1 < 0 || s1 > n_e) || s_end != n_e) return false;
+    // last bucket whose first unit is <= c (buckets may be empty: take the last such start)
+    const unsigned m0 = __ballot_sync(0xffffffffu, s0 * rep <= c);
+    const unsigned m1 = __ballot_sync(0xffffffffu, s1 * rep <= c);
+    const int k = m1 ? 32 + 31 - __clz(m1) : 31 - __clz(m0);
+    if (k < 0 || c >= n_e * rep) return false;
+    const int64_t kb = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
+    const int64_t knext = (k + 1 < kOrderBuckets)
+                              ? __shfl_sync(0xffffffffu, (k + 1) < 32 ? s0 : s1, (k + 1) & 31)
+                              : s_end;
+    const int64_t cnt = knext - kb;
+    if (cnt <= 0 || knext > n_e) return false;
+    const int64_t local = c - kb * rep;
+    const int64_t hr = local / cnt;
+    const int32_t v = order[kb + (local - hr * cnt)];
+    if (v < 0 || (int64_t)v >= n_e) return false;
+    const int s = v / n_tiles;
+    *tile = v - s * n_tiles;
+    *b = s / Hm;
+    *h = (Hm == 1) ? (int)hr : s - *b * Hm;
+    return true;
+}
+#endif
 
 // Arguments of the forward kernel (everything but the TMA descriptors).
 struct FwdArgs {
@@ -97,6 +161,7 @@ enum KernelId {
     kKBwdPre = FM_K_BWD_PRE,
     kKBwd = FM_K_BWD,
     kKBwdPost = FM_K_BWD_POST,
+    kKClassifyOrder = FM_K_CLASSIFY_ORDER,
 };
 
 // Default limit of every bounded device-side wait, in SM clock cycles

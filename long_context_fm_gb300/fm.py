@@ -23,10 +23,11 @@ FM_ERR_BAD_BOUNDS, FM_ERR_PLAN_MISMATCH, FM_ERR_WORKSPACE, FM_ERR_CUDA, FM_ERR_T
 FM_TILE_SKIP, FM_TILE_FULL, FM_TILE_PARTIAL = 0, 1, 2
 FM_DT_BF16, FM_DT_F32 = 0, 1
 FM_FLAG_PRECISE = 1
-KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post"]
+KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post",
+                "classify_order"]
 
-EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_plan_bytes",
-            "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
+EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_mask_from_row_intervals",
+            "fm_plan_bytes", "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
             "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
             "fm_attn_bwd_noalloc"]
 # Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
@@ -54,6 +55,7 @@ _lib.fm_status_string.restype = ctypes.c_char_p
 _lib.fm_status_string.argtypes = [_I]
 _lib.fm_abi_version.restype = _I
 _lib.fm_mask_from_rows.argtypes = [_P, _P, _I, _I, _I, _P, _P, _P, _P]
+_lib.fm_mask_from_row_intervals.argtypes = [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]
 _lib.fm_plan_bytes.restype = _SZ
 _lib.fm_plan_bytes.argtypes = [_I, _I, _I, _I, _I]
 _lib.fm_tile_classify.argtypes = [Bounds, _I, _I, _P, _SZ, _P, _P, _P]
@@ -136,6 +138,21 @@ def fm_mask_from_rows(cs, ce):
     code = _lib.fm_mask_from_rows(cs.ctypes.data, ce.ctypes.data, B, Hm, N,
                                   *[o.ctypes.data for o in out])
     _check(code, "fm_mask_from_rows")
+    return tuple(out)
+
+
+def fm_mask_from_row_intervals(starts, ends):
+    """Host conversion of K inclusive intervals per row (int32 [B, Hm, N, K];
+    start > end marks an unused slot) to column bounds [B, Hm, N]."""
+    starts = np.ascontiguousarray(starts, dtype=np.int32)
+    ends = np.ascontiguousarray(ends, dtype=np.int32)
+    if starts.ndim != 4 or starts.shape != ends.shape:
+        raise ValueError("starts and ends must be int32 [B, Hm, N, K]")
+    B, Hm, N, K = starts.shape
+    out = [np.empty((B, Hm, N), np.int32) for _ in range(4)]
+    code = _lib.fm_mask_from_row_intervals(starts.ctypes.data, ends.ctypes.data, K, B, Hm, N,
+                                           *[o.ctypes.data for o in out])
+    _check(code, "fm_mask_from_row_intervals")
     return tuple(out)
 
 

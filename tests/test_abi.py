@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(fm):
 
 
 def test_abi_version_and_status_strings(fm):
-    assert fm.fm_abi_version() == 2
+    assert fm.fm_abi_version() == 3
     for code in range(9):
         assert fm.fm_status_string(code) and "unknown" not in fm.fm_status_string(code)
     assert "unknown" in fm.fm_status_string(99)
@@ -167,3 +167,121 @@ def test_converter_batches_and_heads(fm):
     got = fm.fm_mask_from_rows(cs2, ce2)
     assert np.array_equal(got[0][:, :1], m["lts"]) and np.array_equal(got[3][:, :1], m["ute"])
     assert np.all(got[3][:, 1] == np.arange(wl.N)) and np.all(got[0][:, 1] == wl.N)
+
+
+# ---- several intervals per row (blog "FlashMask技术" §6.1 item 1) -------------
+@pytest.mark.parametrize("name", [n for n in list(W.SMALL) + ["tiny_causal", "doc_packing",
+                                                             "sliding_window", "prefix_lm",
+                                                             "sliding_window_sink"]])
+def test_interval_converter_reproduces_generator_bounds(fm, name):
+    wl = W.SMALL.get(name) or W.FULL[name]
+    m = W.make_mask(wl)
+    if m["row_intervals"] is None:
+        pytest.skip("no row form")
+    got = fm.fm_mask_from_row_intervals(*m["row_intervals"])
+    for arr, key in zip(got, ("lts", "lte", "uts", "ute")):
+        assert np.array_equal(arr, m[key]), key
+    if m["rows"] is not None:                         # K = 1: same as the one-interval entry
+        ref = fm.fm_mask_from_rows(*m["rows"])
+        assert all(np.array_equal(a, b) for a, b in zip(got, ref))
+
+
+def test_interval_converter_golden_example(fm):
+    import json
+    gd = json.load(open(os.path.join(ROOT, "tests", "golden", "multi_interval_example.json")))
+    N = gd["N"]
+    starts = np.ones((N, 2), np.int32)
+    ends = np.zeros((N, 2), np.int32)
+    for r, ivs in gd["rows"].items():
+        for k, (a, b) in enumerate(ivs):
+            starts[int(r), k], ends[int(r), k] = a, b
+    got = fm.fm_mask_from_row_intervals(starts[None, None], ends[None, None])
+    for j, want in gd["expect_columns"].items():
+        assert [int(g[0, 0, int(j)]) for g in got] == want, j
+    # slots in the other order, and a third slot that overlaps the first
+    s2 = np.concatenate([starts[:, ::-1], starts[:, :1]], axis=1)
+    e2 = np.concatenate([ends[:, ::-1], ends[:, :1]], axis=1)
+    got2 = fm.fm_mask_from_row_intervals(s2[None, None], e2[None, None])
+    assert all(np.array_equal(a, b) for a, b in zip(got, got2))
+
+
+def _row_runs(M):
+    """Attended runs of each row of a dense mask as inclusive (start, end) slots,
+    padded with unused (1, 0) slots to the largest count."""
+    N = M.shape[0]
+    runs = []
+    for i in range(N):
+        a = np.concatenate([[0], (~M[i]).astype(np.int8), [0]])
+        d = np.diff(a)
+        runs.append(list(zip(np.flatnonzero(d == 1), np.flatnonzero(d == -1) - 1)))
+    K = max(1, max(len(r) for r in runs))
+    s = np.ones((N, K), np.int32)
+    e = np.zeros((N, K), np.int32)
+    for i, r in enumerate(runs):
+        for k, (a, b) in enumerate(r):
+            s[i, k], e[i, k] = a, b
+    return s, e
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_interval_converter_round_trips_column_masks(fm, seed):
+    """Any two-range column mask has a row form with several intervals per row;
+    converting that back gives the same dense mask in canonical form."""
+    wl = W.SMALL["random_cols_small"]
+    m = W.make_mask(wl, seed)
+    for b in range(wl.B):
+        for hm in range(wl.Hm):
+            Mc = oracle.dense_from_cols(*_cols(m, b, hm))
+            s, e = _row_runs(Mc)
+            assert s.shape[1] > 1
+            got = fm.fm_mask_from_row_intervals(s[None, None], e[None, None])
+            assert np.array_equal(oracle.dense_from_cols(*[g[0, 0] for g in got]), Mc)
+            lts, lte, uts, ute = (g[0, 0] for g in got)
+            N = wl.N
+            assert np.all((lts < lte) | ((lts == N) & (lte == N)))
+            assert np.all((uts < ute) | ((uts == 0) & (ute == 0)))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_interval_converter_random_rows_against_dense_masks(fm, seed):
+    rng = np.random.default_rng(2000 + seed)
+    N = int(rng.integers(1, 80))
+    K = int(rng.integers(1, 5))
+    mode = seed % 3
+    if mode == 0:       # arbitrary, overlapping, unsorted: often unrepresentable
+        a = rng.integers(0, N, size=(N, K)); b = rng.integers(0, N, size=(N, K))
+        s, e = np.minimum(a, b), np.maximum(a, b)
+    elif mode == 1:     # a sliding structure per slot: usually representable
+        base = np.sort(rng.integers(0, N, size=(N, K)), axis=0)
+        s = base
+        e = np.minimum(N - 1, base + rng.integers(0, 6, size=(1, K)))
+    else:               # with unused slots
+        s = rng.integers(0, N, size=(N, K)); e = s + rng.integers(-4, 8, size=(N, K))
+        e = np.minimum(e, N - 1)
+    s = s.astype(np.int32); e = e.astype(np.int32)
+    Mr = oracle.dense_from_row_intervals(s, e)
+    representable = bool((_masked_runs_per_column(Mr) <= 2).all())
+    try:
+        got = fm.fm_mask_from_row_intervals(s[None, None], e[None, None])
+    except fm.FmError as err:
+        assert err.code == fm.FM_ERR_UNREPRESENTABLE and not representable
+        return
+    assert representable
+    assert np.array_equal(Mr, oracle.dense_from_cols(*[g[0, 0] for g in got]))
+
+
+def test_interval_converter_rejects_bad_input(fm):
+    s = np.array([[[[0, 2], [1, 5]]]], np.int32)      # [1, 1, 2, 2]: slot (5, ...) too far
+    e = np.array([[[[0, 1], [1, 5]]]], np.int32)
+    with pytest.raises(fm.FmError) as err:
+        fm.fm_mask_from_row_intervals(s, e)
+    assert err.value.code == fm.FM_ERR_BAD_BOUNDS
+    s = np.array([[[[0, -1], [1, 3]]]], np.int32)
+    e = np.array([[[[0, 0], [1, 2]]]], np.int32)      # (-1, 0) used with a negative start
+    with pytest.raises(fm.FmError) as err:
+        fm.fm_mask_from_row_intervals(s, e)
+    assert err.value.code == fm.FM_ERR_BAD_BOUNDS
+    z = np.zeros(4, np.int32)
+    p = z.ctypes.data
+    assert fm._lib.fm_mask_from_row_intervals(p, p, 0, 1, 1, 2, p, p, p, p) == fm.FM_ERR_INVALID_ARG
+    assert fm._lib.fm_mask_from_row_intervals(None, p, 1, 1, 1, 2, p, p, p, p) == fm.FM_ERR_INVALID_ARG

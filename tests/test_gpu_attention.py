@@ -191,5 +191,6 @@ def test_profiler_records_every_launch(fm):
     run_fm(fm, wl, m, q, k, v, dO)
     rec = fm.fm_profile_end()
     names = [r[0] for r in rec]
-    assert names == ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post"]
+    assert names == ["classify_minmax", "classify_lists", "classify_order", "fwd", "bwd_pre", "bwd",
+                     "bwd_post"]
     assert all(ms > 0 for _, ms in rec)

@@ -65,3 +65,47 @@ def test_host_argument_errors(fm):
     with pytest.raises(fm.FmError) as e:
         fm.fm_tile_classify(att.bounds, att.plan, att.status, bq=96)
     assert e.value.code == fm.FM_ERR_INVALID_ARG
+
+
+def _bucket(n):
+    """Length bucket of a work list: half-octaves, longest first, empty lists last."""
+    n = np.asarray(n, np.int64)
+    lg = np.where(n > 0, np.floor(np.log2(np.maximum(n, 1))), 0).astype(np.int64)
+    half = np.where(lg > 0, (n >> np.maximum(lg - 1, 0)) & 1, 0)
+    return np.where(n > 0, 62 - (2 * lg + half), 63)
+
+
+def test_bucket_rule_is_monotone():
+    n = np.arange(0, 1 << 16)
+    b = _bucket(n)
+    assert b[0] == 63 and b[1] == 62 and b[2] == 60 and b[3] == 59 and b[256] == 46
+    assert np.all(np.diff(b[1:]) <= 0)
+
+
+@pytest.mark.parametrize("name", ["causal_ragged", "docs_small", "window_sink_small", "random_cols_small",
+                                  "random_cols_d64", "all_masked_small", "long_packing_128k",
+                                  "sliding_window_sink"])
+def test_work_order_longest_first_and_stable(fm, name):
+    """The plan's two work orders (read at the offsets its header records) are
+    the stable sorts, longest bucket first, of the non-skip counts of the
+    oracle's labels: per (b, hm, Q tile) for the forward and per (b, hm, KV
+    tile) for the backward, entries s * n_tiles + tile; the bucket starts
+    delimit the buckets."""
+    wl = W.SMALL.get(name) or W.FULL[name]
+    m = W.make_mask(wl)
+    att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"])
+    torch.cuda.synchronize()
+    att.check_status()
+    plan = att.plan.cpu().numpy()
+    hdr = plan[:128]
+    n_q, n_k = (int(x) for x in hdr[24:32].view(np.int32))
+    off_row, off_col, off_rb, off_cb = (int(x) for x in hdr[40:72].view(np.int64))
+    ref = oracle.tile_labels_all(m, 128, 128)                  # [B, Hm, n_q, n_k]
+    S = wl.B * wl.Hm
+    for cnt, off, offb, n_t in (((ref != oracle.SKIP).sum(axis=3).reshape(S * n_q), off_row, off_rb, n_q),
+                                ((ref != oracle.SKIP).sum(axis=2).reshape(S * n_k), off_col, off_cb, n_k)):
+        bkt = _bucket(cnt)
+        got = plan[off:off + 4 * S * n_t].view(np.int32)
+        assert np.array_equal(got, np.argsort(bkt, kind="stable"))
+        starts = plan[offb:offb + 4 * 65].view(np.int32)
+        assert np.array_equal(starts, np.concatenate([[0], np.cumsum(np.bincount(bkt, minlength=64))]))
