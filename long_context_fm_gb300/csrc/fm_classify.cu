@@ -185,23 +185,30 @@ __global__ void __launch_bounds__(kOrderThreads) classify_order_kernel(PlanLayou
         bstart[kOrderBuckets] = run;
     }
     __syncthreads();
-    // stable scatter: chunks in index order, the warps of a chunk one after another
+    // stable scatter, one chunk of 1024 entries at a time: rank inside the warp
+    // (peers with the same bucket), then a scan of the warps' counts per bucket.
+    __shared__ uint8_t wcnt[kOrderThreads / 32][kOrderBuckets];
+    __shared__ int wbase[kOrderThreads / 32][kOrderBuckets];
     for (int64_t c0 = 0; c0 < n_e; c0 += kOrderThreads) {
+        for (int i = t; i < (kOrderThreads / 32) * kOrderBuckets; i += kOrderThreads) (&wcnt[0][0])[i] = 0;
+        __syncthreads();
         const int64_t e = c0 + t;
         const int bk = e < n_e ? order_bucket(len[e]) : -1;
-        for (int ww = 0; ww < kOrderThreads / 32; ++ww) {
-            if (w == ww) {
-                const unsigned peers = __match_any_sync(0xffffffffu, bk);
-                const int rank = __popc(peers & ((1u << ln) - 1u));
-                const int base = bk >= 0 ? next[bk] : 0;
-                __syncwarp();
-                if (bk >= 0) {
-                    order[base + rank] = (int32_t)e;
-                    if (rank == 0) next[bk] = base + __popc(peers);
-                }
+        const unsigned peers = __match_any_sync(0xffffffffu, bk);
+        const int rank = __popc(peers & ((1u << ln) - 1u));
+        if (bk >= 0 && rank == 0) wcnt[w][bk] = (uint8_t)__popc(peers);
+        __syncthreads();
+        if (t < kOrderBuckets) {
+            int run = next[t];
+            for (int ww = 0; ww < kOrderThreads / 32; ++ww) {
+                wbase[ww][t] = run;
+                run += wcnt[ww][t];
             }
-            __syncthreads();
+            next[t] = run;
         }
+        __syncthreads();
+        if (bk >= 0) order[wbase[w][bk] + rank] = (int32_t)e;
+        __syncthreads();
     }
 }
 
