@@ -49,9 +49,9 @@ struct FwdSmem {
     static constexpr int kV = kK + kKStages * kTile;           // [kVStages]
     static constexpr int kBnd = kV + kVStages * kTile;         // int4 [kVStages][128]
     static constexpr int kMax = kBnd + kVStages * 128 * 16;    // float [2 slots][2 warpgroups][128]
-    static constexpr int kSum = kMax + 2 * 2 * 128 * 4;        // float [2 warpgroups][2][128]: l, rounded l
+    static constexpr int kSum = kMax + 2 * 2 * 128 * 4;        // float [2 warpgroups][128]: l
     static constexpr int kListCap = 2048;                      // KV tiles staged from the plan
-    static constexpr int kList = kSum + 2 * 2 * 128 * 4;
+    static constexpr int kList = kSum + 2 * 128 * 4;
     static constexpr int kBar = kList + kListCap * 4;
     static constexpr int kNumBar = 22;
     static constexpr int kMisc = kBar + kNumBar * 8;
@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(352, 1)
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const uint32_t tO = tmem + 384;
             constexpr int OC = D / 2;                  // O columns rescaled / stored by this warpgroup
-            float m = -INFINITY, l = 0.f, lr = 0.f;
+            float m = -INFINITY, l = 0.f;
             // `live` turns false (for the whole warp) when a wait gives up after an
             // abort; the warp then skips its work but still reaches every named
             // barrier of the loop, so the other warpgroup is never left waiting.
@@ -385,12 +385,14 @@ __global__ void __launch_bounds__(352, 1)
                 }
                 // P = exp2(s * scale*log2e - m) as packed bf16 over the S buffer:
                 // this warpgroup's 64 columns go to TMEM columns [32 w, 32 w + 32)
-                // (precise mode: P_lo to [64 + 32 w, ...)).  Standard mode
-                // normalises O by the sum of the rounded P (the weights the PV
-                // product really applied); lse uses the fp32 sum.  Column pairs in
-                // packed fp32.
+                // (precise mode: P_lo to [64 + 32 w, ...)).  O is normalised by the
+                // fp32 sum of P, which also gives lse (standard mode: the bf16
+                // rounding of the weights P V applied moves that sum by ~2^-9
+                // relative at most, far inside the tolerance, and summing the
+                // rounded values instead costs 1.5 instructions per element on
+                // the critical chain).  Column pairs in packed fp32.
                 const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-m_use, -m_use);
-                uint64_t sum2 = f2_pack(0.f, 0.f), rs2 = f2_pack(0.f, 0.f);
+                uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t hi[16], lo[16];
@@ -404,8 +406,6 @@ __global__ void __launch_bounds__(352, 1)
                         if (PRECISE) {
                             lo[cc] = pack_bf16x2(p0 - __uint_as_float(hi[cc] << 16),
                                                  p1 - __uint_as_float(hi[cc] & 0xffff0000u));
-                        } else {
-                            rs2 = f2_add(rs2, f2_pack(__uint_as_float(hi[cc] << 16), __uint_as_float(hi[cc] & 0xffff0000u)));
                         }
                     }
                     tmem_st16(tS + lane_off + w * 32 + hh * 16, hi);
@@ -414,10 +414,6 @@ __global__ void __launch_bounds__(352, 1)
                 float s0, s1;
                 f2_unpack(sum2, s0, s1);
                 l = l * alpha + (s0 + s1);
-                if (!PRECISE) {
-                    f2_unpack(rs2, s0, s1);
-                    lr = lr * alpha + (s0 + s1);
-                }
                 m = m_new;
                 tmem_st_wait();
                 tc_fence_before();
@@ -427,16 +423,13 @@ __global__ void __launch_bounds__(352, 1)
             // Combine the two warpgroups' partial sums (one more named barrier,
             // reached by every thread of both), then each stores its half of O
             // after the last PV.
-            sSum[(w * 2 + 0) * 128 + r] = l;
-            sSum[(w * 2 + 1) * 128 + r] = lr;
+            sSum[w * 128 + r] = l;
             named_bar_sync(kSoftmaxBar, 256);
             if (n > 0) wait_pv(n - 1);
             if (live) {
                 tc_fence_after();
-                const float lt = sSum[0 * 128 + r] + sSum[2 * 128 + r];
-                const float lrt = sSum[1 * 128 + r] + sSum[3 * 128 + r];
-                const float nrm = PRECISE ? lt : lrt;
-                const float inv = (nrm > 0.f) ? 1.f / nrm : 0.f;
+                const float lt = sSum[r] + sSum[128 + r];
+                const float inv = (lt > 0.f) ? 1.f / lt : 0.f;
                 const bool row_in = i < N;
                 const int64_t row = (int64_t)bh * N + i;
 #pragma unroll

@@ -75,10 +75,13 @@ def test_single_row_and_tiny_n(fm):
             check_close(key, out[key].cpu().numpy(), g[key])
 
 
-def test_constant_v_and_dead_rows(fm):
+@pytest.mark.parametrize("precise", [False, True])
+def test_constant_v_and_dead_rows(fm, precise):
     """Constant V returns V on every row that attends something; rows that
     attend nothing return O = 0 and lse = -inf; columns nobody attends get
-    dK = dV = 0."""
+    dK = dV = 0.  O = sum_j p^_j v / sum_j p_j: the product applies the bf16
+    weights p^_j = p_j (1 + e_j), |e_j| <= 2^-9, so standard mode returns V
+    within 2^-9 relative; precise mode (p^ = hi + lo) within ~2^-17."""
     N, d = 300, 128
     lts = np.full(N, N, np.int32); lte = np.full(N, N, np.int32)
     uts = np.zeros(N, np.int32); ute = np.maximum(np.arange(N), 150).astype(np.int32)
@@ -90,13 +93,13 @@ def test_constant_v_and_dead_rows(fm):
     q, k, dO = (torch.randn(1, 2, N, d, generator=g).to(torch.bfloat16) for _ in range(3))
     vrow = torch.randn(d, generator=g).to(torch.bfloat16)
     v = vrow.expand(1, 2, N, d).contiguous()
-    out = run_fm(fm, wl, m, q, k, v, dO)
+    out = run_fm(fm, wl, m, q, k, v, dO, flags=fm.FM_FLAG_PRECISE if precise else 0)
     M = oracle.dense_from_cols(lts, lte, uts, ute)
     live = ~M.all(1)
     o = out["o"].cpu().numpy()[0]
     assert (~live).sum() == 50                               # rows 100..149 see nothing
-    np.testing.assert_allclose(o[:, live], np.broadcast_to(vrow.float().numpy(), (2, live.sum(), d)),
-                               atol=1e-5)
+    want = np.broadcast_to(vrow.float().numpy(), (2, live.sum(), d))
+    np.testing.assert_allclose(o[:, live], want, rtol=(1e-5 if precise else 2.0 ** -9), atol=1e-6)
     assert np.all(o[:, ~live] == 0)
     assert np.all(out["lse"].cpu().numpy()[0, :, ~live] == -np.inf)
     assert np.all(out["dq"].cpu().numpy()[0, :, ~live] == 0)
