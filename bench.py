@@ -9,7 +9,9 @@ backward, 14d together); `value` is the fwd+bwd figure with inputs resident
 in HBM.  `e2e` repeats the step through the C ABI from pinned host buffers:
 row-form mask conversion on the host, host-to-device copies of Q, K, V, dO
 and the bounds, the device work, and device-to-host copies of O, lse, dQ,
-dK, dV, all inside the timed region.
+dK, dV, all inside the timed region.  `graph` times the same step captured
+once into a CUDA graph (fm_step_graph_create) and replayed, one launch per
+step.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fm|reference]
 Under torchrun every rank runs the whole workload on its own GPU (independent
@@ -206,6 +208,23 @@ def run_fm(args, rank, world, local_rank):
     avg = {kname: sum(v_) / len(v_) for kname, v_ in per_kernel.items()}
     launches = len(recs)
 
+    # ---- the same step replayed from a captured graph (one launch per step)
+    gh = fm.fm_step_graph_create(q, k, v, dO, bounds, plan, scale, o, lse, status, dq, dk, dv, ws)
+    for _ in range(2):
+        fm.fm_step_graph_launch(gh, stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        fm.fm_step_graph_launch(gh, stream)
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    graph_ms = g0.elapsed_time(g1) / args.steps
+    fm.fm_step_graph_destroy(gh)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in graph replay")
+
     # ---- end to end through the C ABI from pinned host buffers
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dO))
     rows = m["rows"]
@@ -244,9 +263,10 @@ def run_fm(args, rank, world, local_rank):
     barrier()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
 
-    ms_step, e2e_s = max_over_ranks([ms_step, e2e_s], world, dev)
+    ms_step, e2e_s, graph_ms = max_over_ranks([ms_step, e2e_s, graph_ms], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
-                avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h)
+                avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h,
+                graph_ms=graph_ms)
 
 
 def mask_description(wl):
@@ -371,6 +391,9 @@ def main():
                          "peak": peak_sus, "unit": "TFLOP/s", "frac": bwd_tflops / peak_sus,
                          "traffic": traffic, "peak_source": f"{src} bf16 sustained"},
             "gpu_launches": r["launches"],
+            "graph": {"ms_per_step": r["graph_ms"], "value": world * step_flops / (r["graph_ms"] * 1e-3) / 1e12,
+                      "unit": "TFLOP/s", "launches_per_step": 1,
+                      "note": "the same step captured once (fm_step_graph_create) and replayed"},
             "clocks": r["clocks"],
             "e2e": {"value": world * step_flops / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

@@ -227,6 +227,46 @@ FM_API fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const void *v
                                      int32_t *dev_status, fm_stream_t stream);
 
 /*
+ * Step graphs — create / destroy HOST, synchronous; launch DEVICE, async.
+ * One step of the path (fm_tile_classify, fm_attn_fwd and, when dO is given,
+ * fm_attn_bwd; 128 x 128 tiles) captured once into a CUDA graph for a fixed
+ * set of buffers and replayed with a single launch.  Passages: blog §6.2
+ * item 1 (capture the compute pattern in a CUDA Graph) and FlashAttention
+ * article §三.3 (CUDA Graphs to cut kernel-launch overhead, which dominates
+ * small problems).  Every launch reads the current contents of
+ * the buffers in fm_step_args: refill q, k, v, dO and the bounds in place
+ * between launches.  The caller keeps every buffer allocated and unmoved until
+ * fm_step_graph_destroy, zeroes dev_status before reading it, and does not run
+ * two launches on the same buffers concurrently.
+ * fm_step_graph_create: argument errors are those of the three calls (the
+ * capture is discarded, nothing is allocated); args or graph NULL ->
+ * FM_ERR_INVALID_ARG; a failed capture -> FM_ERR_CUDA.  *graph is written on
+ * success only (else set to NULL).
+ */
+typedef struct {
+    const void *q, *k, *v;          /* bf16 [B, H, N, d] */
+    const void *dO;                 /* bf16 [B, H, N, d], or NULL: forward-only graph */
+    fm_bounds mask;
+    void *plan;                     /* fm_plan_bytes(B, Hm, N, 128, 128) bytes */
+    size_t plan_bytes;
+    void *o;                        /* [B, H, N, d] of o_dtype */
+    int o_dtype;
+    float *lse;                     /* [B, H, N] */
+    void *dq, *dk, *dv;             /* [B, H, N, d] of grad_dtype; unused without dO */
+    int grad_dtype;
+    void *ws;                       /* fm_bwd_workspace_bytes(B, H, N, d); unused without dO */
+    size_t ws_bytes;
+    int B, H, N, d;
+    float scale;
+    int flags;                      /* FM_FLAG_PRECISE or 0 */
+    int32_t *dev_status;
+} fm_step_args;
+typedef struct fm_step_graph_st *fm_step_graph;
+FM_API fm_status fm_step_graph_create(const fm_step_args *args, fm_step_graph *graph);
+FM_API fm_status fm_step_graph_launch(fm_step_graph graph, fm_stream_t stream);
+FM_API fm_status fm_step_graph_destroy(fm_step_graph graph);
+
+/*
  * Per-kernel timing (the library's own tracing).  fm_profile_begin starts
  * recording a CUDA event pair around every kernel the library launches
  * (process-wide, up to 4096 launches); fm_profile_end waits for those

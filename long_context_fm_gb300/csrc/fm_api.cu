@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "fm_internal.h"
@@ -22,6 +23,8 @@ fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dou
                             int64_t rows, int d, cudaStream_t stream);
 fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,
                              cudaStream_t stream);
+fm_status fm_fwd_prepare(int d, bool precise);
+fm_status fm_bwd_prepare(int d, bool precise);
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const FwdArgs &a, int d, bool precise, cudaStream_t stream);
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -30,7 +33,7 @@ fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 
 bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
 
@@ -119,6 +122,10 @@ ProfScope::ProfScope(int kernel, void *st) : slot(-1), stream(st)
 {
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on || g_prof.size() >= kProfMax) return;
+    // Launches being captured into a graph are not timed (their events would
+    // become graph nodes).
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing((cudaStream_t)st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
     ProfRec r{kernel, nullptr, nullptr};
     if (cudaEventCreate(&r.a) != cudaSuccess) return;
     if (cudaEventCreate(&r.b) != cudaSuccess) {
@@ -284,6 +291,74 @@ fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o
     if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
         return st;
     return fm_bwd_post_launch(dq_acc, dq, grad_dtype == FM_DT_F32, scale, rows * d, s);
+}
+
+struct fm_step_graph_st {
+    cudaGraphExec_t exec;
+};
+
+fm_status fm_step_graph_create(const fm_step_args *a, fm_step_graph *graph)
+{
+    if (!graph) return FM_ERR_INVALID_ARG;
+    *graph = nullptr;
+    if (!a) return FM_ERR_INVALID_ARG;
+    // Everything that is not a stream operation happens before the capture:
+    // device check, the driver's tensor-map entry point, kernel attributes.
+    fm_status st = check_device();
+    if (st != FM_OK) return st;
+    if (!encode_fn()) return FM_ERR_CUDA;
+    if (a->d != 64 && a->d != 128) return FM_ERR_UNSUPPORTED;
+    const bool precise = (a->flags & FM_FLAG_PRECISE) != 0;
+    if ((st = fm_fwd_prepare(a->d, precise)) != FM_OK) return st;
+    if (a->dO && (st = fm_bwd_prepare(a->d, precise)) != FM_OK) return st;
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return FM_ERR_CUDA;
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaStreamDestroy(s);
+        return FM_ERR_CUDA;
+    }
+    const fm_stream_t fs = (fm_stream_t)s;
+    st = fm_tile_classify(a->mask, 128, 128, a->plan, a->plan_bytes, nullptr, a->dev_status, fs);
+    if (st == FM_OK)
+        st = fm_attn_fwd(a->q, a->k, a->v, a->mask, a->plan, a->B, a->H, a->N, a->d, a->scale, a->o, a->o_dtype,
+                         a->lse, nullptr, 0, a->flags, a->dev_status, fs);
+    if (st == FM_OK && a->dO)
+        st = fm_attn_bwd(a->q, a->k, a->v, a->o, a->o_dtype, a->lse, a->dO, a->mask, a->plan, a->B, a->H, a->N,
+                         a->d, a->scale, a->dq, a->dk, a->dv, a->grad_dtype, a->flags, a->ws, a->ws_bytes,
+                         a->dev_status, fs);
+    cudaGraph_t g = nullptr;
+    const cudaError_t ec = cudaStreamEndCapture(s, &g);
+    if (st == FM_OK && (ec != cudaSuccess || !g)) st = FM_ERR_CUDA;
+    cudaGraphExec_t exec = nullptr;
+    if (st == FM_OK && cudaGraphInstantiate(&exec, g, 0) != cudaSuccess) st = FM_ERR_CUDA;
+    if (g) cudaGraphDestroy(g);
+    cudaStreamDestroy(s);
+    if (st != FM_OK) {
+        if (exec) cudaGraphExecDestroy(exec);
+        cudaGetLastError();   // a failed capture leaves no sticky error for the caller
+        return st;
+    }
+    fm_step_graph h = new (std::nothrow) fm_step_graph_st{exec};
+    if (!h) {
+        cudaGraphExecDestroy(exec);
+        return FM_ERR_CUDA;
+    }
+    *graph = h;
+    return FM_OK;
+}
+
+fm_status fm_step_graph_launch(fm_step_graph graph, fm_stream_t stream)
+{
+    if (!graph) return FM_ERR_INVALID_ARG;
+    return cudaGraphLaunch(graph->exec, (cudaStream_t)stream) == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_step_graph_destroy(fm_step_graph graph)
+{
+    if (!graph) return FM_ERR_INVALID_ARG;
+    const cudaError_t e = cudaGraphExecDestroy(graph->exec);
+    delete graph;
+    return e == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status fm_profile_begin(void)

@@ -37,6 +37,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fm_internal.h"
 #include "fm_ptx.cuh"
 
@@ -619,19 +621,41 @@ fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dou
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
+// The kernel's shared-memory limit, set once per device: later launches (also
+// those captured into a graph) make no attribute call.
+template <int D, bool PRECISE>
+static bool bwd_smem_ready()
+{
+    constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    static std::atomic<uint8_t> done[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (done[dev].load(std::memory_order_acquire)) return true;
+    if (cudaFuncSetAttribute(fm_bwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return false;
+    done[dev].store(1, std::memory_order_release);
+    return true;
+}
+
 template <int D, bool PRECISE>
 static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const CUtensorMap &tdo, const BwdArgs &a,
                             cudaStream_t stream)
 {
     constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
-    static_assert(smem <= 227 * 1024, "shared memory budget");
-    if (cudaFuncSetAttribute(fm_bwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return FM_ERR_CUDA;
+    if (!bwd_smem_ready<D, PRECISE>()) return FM_ERR_CUDA;
     ProfScope ps(kKBwd, stream);
     fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 736, smem, stream>>>(tq, tk, tv, tdo, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_bwd_prepare(int d, bool precise)
+{
+    const bool ok = d == 128 ? (precise ? bwd_smem_ready<128, true>() : bwd_smem_ready<128, false>())
+                             : (precise ? bwd_smem_ready<64, true>() : bwd_smem_ready<64, false>());
+    return ok ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

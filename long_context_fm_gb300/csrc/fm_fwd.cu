@@ -34,6 +34,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "fm_internal.h"
 #include "fm_ptx.cuh"
 
@@ -478,18 +480,40 @@ __global__ void __launch_bounds__(352, 1)
 
 using namespace fm;
 
+// The kernel's shared-memory limit, set once per device: later launches (also
+// those captured into a graph) make no attribute call.
+template <int D, bool PRECISE>
+static bool fwd_smem_ready()
+{
+    constexpr int smem = FwdSmem<D>::kBytes;
+    static_assert(smem <= 227 * 1024, "shared memory budget");
+    static std::atomic<uint8_t> done[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (done[dev].load(std::memory_order_acquire)) return true;
+    if (cudaFuncSetAttribute(fm_fwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+        return false;
+    done[dev].store(1, std::memory_order_release);
+    return true;
+}
+
 template <int D, bool PRECISE>
 static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdArgs &a, cudaStream_t stream)
 {
     constexpr int smem = FwdSmem<D>::kBytes;
-    static_assert(smem <= 227 * 1024, "shared memory budget");
-    if (cudaFuncSetAttribute(fm_fwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return FM_ERR_CUDA;
+    if (!fwd_smem_ready<D, PRECISE>()) return FM_ERR_CUDA;
     ProfScope ps(kKFwd, stream);
     fm_fwd_kernel<D, PRECISE><<<dim3(a.L.n_q, a.H, a.B), 352, smem, stream>>>(tq, tk, tv, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_fwd_prepare(int d, bool precise)
+{
+    const bool ok = d == 128 ? (precise ? fwd_smem_ready<128, true>() : fwd_smem_ready<128, false>())
+                             : (precise ? fwd_smem_ready<64, true>() : fwd_smem_ready<64, false>());
+    return ok ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

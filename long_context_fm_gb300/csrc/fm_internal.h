@@ -164,6 +164,9 @@ enum KernelId {
     kKClassifyOrder = FM_K_CLASSIFY_ORDER,
 };
 
+// Devices a process may use (per-device caches of kernel attributes).
+constexpr int kMaxDevices = 64;
+
 // Default limit of every bounded device-side wait, in SM clock cycles
 // (about 1.5 s at 1.4-2.1 GHz): far above any legitimate wait inside a CTA.
 constexpr long long kWaitLimitCycles = 3000000000LL;

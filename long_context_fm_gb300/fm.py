@@ -29,7 +29,7 @@ KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "b
 EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_mask_from_row_intervals",
             "fm_plan_bytes", "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
             "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
-            "fm_attn_bwd_noalloc"]
+            "fm_attn_bwd_noalloc", "fm_step_graph_create", "fm_step_graph_launch", "fm_step_graph_destroy"]
 # Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -44,6 +44,18 @@ class Bounds(ctypes.Structure):
     _fields_ = [("lts", ctypes.c_void_p), ("lte", ctypes.c_void_p), ("uts", ctypes.c_void_p),
                 ("ute", ctypes.c_void_p), ("B", ctypes.c_int32), ("Hm", ctypes.c_int32),
                 ("N", ctypes.c_int32)]
+
+
+class StepArgs(ctypes.Structure):
+    """fm_step_args of include/fm.h (field order and C layout)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("dO", ctypes.c_void_p), ("mask", Bounds), ("plan", ctypes.c_void_p),
+                ("plan_bytes", ctypes.c_size_t), ("o", ctypes.c_void_p), ("o_dtype", ctypes.c_int),
+                ("lse", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p),
+                ("dv", ctypes.c_void_p), ("grad_dtype", ctypes.c_int), ("ws", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t), ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
+                ("d", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_int),
+                ("dev_status", ctypes.c_void_p)]
 
 
 class KernelTime(ctypes.Structure):
@@ -72,6 +84,9 @@ _lib.fm_profile_begin.argtypes = []
 _lib.fm_profile_end.restype = _I
 _lib.fm_profile_end.argtypes = [_P, _I]
 _lib.fm_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _P, _P]
+_lib.fm_step_graph_create.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(ctypes.c_void_p)]
+_lib.fm_step_graph_launch.argtypes = [_P, _P]
+_lib.fm_step_graph_destroy.argtypes = [_P]
 
 
 def _check(code, where):
@@ -258,6 +273,67 @@ def fm_selftest_wait_timeout(limit_cycles, dev_status, stream=None):
 # Convenience layer: allocates the caller-owned buffers with torch and calls
 # the entry points above.
 # ---------------------------------------------------------------------------
+def fm_step_graph_create(q, k, v, dO, bounds: Bounds, plan, scale, o, lse, dev_status, dq=None, dk=None,
+                         dv=None, ws=None, flags=0):
+    """Capture classify + forward (+ backward when dO is given) for these
+    buffers; returns the opaque handle (an int)."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, torch.bfloat16, n)
+    B, H, N, d = q.shape
+    a = StepArgs()
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.dO = None if dO is None else _dev(dO, torch.bfloat16, "dO").data_ptr()
+    a.mask = bounds
+    a.plan, a.plan_bytes = _dev(plan, torch.uint8, "plan").data_ptr(), plan.numel()
+    a.o, a.o_dtype = _dev(o, o.dtype, "o").data_ptr(), _dt(o)
+    a.lse = _dev(lse, torch.float32, "lse").data_ptr()
+    if dO is not None:
+        if not (dq.dtype == dk.dtype == dv.dtype):
+            raise TypeError("dq, dk, dv must share one dtype")
+        a.dq, a.dk, a.dv = (_dev(t, t.dtype, n).data_ptr() for n, t in (("dq", dq), ("dk", dk), ("dv", dv)))
+        a.grad_dtype = _dt(dq)
+        a.ws, a.ws_bytes = _dev(ws, torch.uint8, "ws").data_ptr(), ws.numel()
+    a.B, a.H, a.N, a.d = B, H, N, d
+    a.scale, a.flags = float(scale), int(flags)
+    a.dev_status = _dev(dev_status, torch.int32, "dev_status").data_ptr()
+    h = ctypes.c_void_p()
+    _check(_lib.fm_step_graph_create(ctypes.byref(a), ctypes.byref(h)), "fm_step_graph_create")
+    return h.value
+
+
+def fm_step_graph_launch(graph, stream=None):
+    _check(_lib.fm_step_graph_launch(ctypes.c_void_p(graph), _stream(stream)), "fm_step_graph_launch")
+
+
+def fm_step_graph_destroy(graph):
+    _check(_lib.fm_step_graph_destroy(ctypes.c_void_p(graph)), "fm_step_graph_destroy")
+
+
+class StepGraph:
+    """One captured step over fixed buffers (keeps them referenced while the
+    graph lives); refill the inputs in place and call launch()."""
+
+    def __init__(self, q, k, v, dO, att: "MaskedAttention", scale, o, lse, dq=None, dk=None, dv=None, ws=None,
+                 flags=0):
+        self._keep = (q, k, v, dO, att, o, lse, dq, dk, dv, ws)
+        self.handle = fm_step_graph_create(q, k, v, dO, att.bounds, att.plan, scale, o, lse, att.status,
+                                           dq, dk, dv, ws, flags)
+
+    def launch(self, stream=None):
+        fm_step_graph_launch(self.handle, stream)
+
+    def close(self):
+        if self.handle is not None:
+            fm_step_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class MaskedAttention:
     """Holds the device bounds, plan and status word of one mask."""
 

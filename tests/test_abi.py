@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(fm):
 
 
 def test_abi_version_and_status_strings(fm):
-    assert fm.fm_abi_version() == 3
+    assert fm.fm_abi_version() == 4
     for code in range(9):
         assert fm.fm_status_string(code) and "unknown" not in fm.fm_status_string(code)
     assert "unknown" in fm.fm_status_string(99)
@@ -285,3 +285,15 @@ def test_interval_converter_rejects_bad_input(fm):
     p = z.ctypes.data
     assert fm._lib.fm_mask_from_row_intervals(p, p, 0, 1, 1, 2, p, p, p, p) == fm.FM_ERR_INVALID_ARG
     assert fm._lib.fm_mask_from_row_intervals(None, p, 1, 1, 1, 2, p, p, p, p) == fm.FM_ERR_INVALID_ARG
+
+
+def test_step_graph_null_arguments(fm):
+    """Argument checks that need no GPU: no graph handle or no arguments."""
+    import ctypes
+    h = ctypes.c_void_p(1234)
+    assert fm._lib.fm_step_graph_create(None, ctypes.byref(h)) == fm.FM_ERR_INVALID_ARG
+    assert h.value is None                                   # cleared on failure
+    assert fm._lib.fm_step_graph_create(ctypes.byref(fm.StepArgs()), None) == fm.FM_ERR_INVALID_ARG
+    assert fm._lib.fm_step_graph_launch(None, None) == fm.FM_ERR_INVALID_ARG
+    assert fm._lib.fm_step_graph_destroy(None) == fm.FM_ERR_INVALID_ARG
+    assert ctypes.sizeof(fm.StepArgs) == 200                 # the C layout on LP64
