@@ -227,6 +227,38 @@ FM_API fm_status fm_attn_bwd_noalloc(const void *q, const void *k, const void *v
                                      int32_t *dev_status, fm_stream_t stream);
 
 /*
+ * Row windows — the same three calls for the Q rows [q_row0, q_row0 + Nq) of
+ * the N x N mask against all N key columns: one rank's share of a sequence
+ * split over several GPUs (blog §4.3, sequence-parallel integration: the
+ * column intervals all-gathered, each rank computing the rows it holds;
+ * key/value shards a window's rows never attend are skipped whole by the
+ * tile labels).  q_row0 must be a multiple of 128 (of bq for
+ * fm_tile_classify_rows), 1 <= Nq, q_row0 + Nq <= N; else FM_ERR_INVALID_ARG.
+ * The bounds keep the whole mask ([B, Hm, N], global row numbers).
+ *   Q, dO, O: [B, H, Nq, d]; lse: [B, H, Nq]; K, V: [B, H, N, d].
+ *   fm_attn_bwd_rows: dQ [B, H, Nq, d] is complete; dK, dV [B, H, N, d]
+ *   receive this window's contribution only (zero where it attends nothing):
+ *   the contributions of all windows add up to the full gradients.  The
+ *   workspace is fm_bwd_workspace_bytes(B, H, Nq, d).
+ * The plan of a window is fm_plan_bytes_rows(...) bytes and is built by
+ * fm_tile_classify_rows with the same window.  Whole mask: q_row0 = 0, Nq = N
+ * (what fm_plan_bytes, fm_tile_classify, fm_attn_fwd and fm_attn_bwd do).
+ */
+FM_API size_t fm_plan_bytes_rows(int B, int Hm, int N, int q_row0, int Nq, int bq, int bk);
+FM_API fm_status fm_tile_classify_rows(fm_bounds m, int q_row0, int Nq, int bq, int bk, void *plan,
+                                size_t plan_bytes, uint8_t *labels, int32_t *dev_status,
+                                fm_stream_t stream);
+FM_API fm_status fm_attn_fwd_rows(const void *q, const void *k, const void *v, fm_bounds m,
+                           const void *plan, int B, int H, int N, int q_row0, int Nq, int d,
+                           float scale, void *o, int o_dtype, float *lse, void *ws, size_t ws_bytes,
+                           int flags, int32_t *dev_status, fm_stream_t stream);
+FM_API fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const void *o,
+                           int o_dtype, const float *lse, const void *dO, fm_bounds m,
+                           const void *plan, int B, int H, int N, int q_row0, int Nq, int d,
+                           float scale, void *dq, void *dk, void *dv, int grad_dtype, int flags,
+                           void *ws, size_t ws_bytes, int32_t *dev_status, fm_stream_t stream);
+
+/*
  * Step graphs — create / destroy HOST, synchronous; launch DEVICE, async.
  * One step of the path (fm_tile_classify, fm_attn_fwd and, when dO is given,
  * fm_attn_bwd; 128 x 128 tiles) captured once into a CUDA graph for a fixed

@@ -17,7 +17,7 @@
 using namespace fm;
 
 // Launchers in the kernel translation units.
-fm_status fm_classify_launch(fm_bounds m, int bq, int bk, void *plan, uint8_t *labels,
+fm_status fm_classify_launch(fm_bounds m, int q_row0, int Nq, int bq, int bk, void *plan, uint8_t *labels,
                              int32_t *status, cudaStream_t stream);
 fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dout, float *dq_acc,
                             int64_t rows, int d, cudaStream_t stream);
@@ -33,7 +33,7 @@ fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const
 
 namespace {
 
-constexpr int kAbiVersion = 4;
+constexpr int kAbiVersion = 5;
 
 bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
 
@@ -180,18 +180,23 @@ const char *fm_status_string(fm_status st)
 
 int fm_abi_version(void) { return kAbiVersion; }
 
-size_t fm_plan_bytes(int B, int Hm, int N, int bq, int bk)
+size_t fm_plan_bytes_rows(int B, int Hm, int N, int q_row0, int Nq, int bq, int bk)
 {
     PlanLayout L;
-    if (!plan_layout(B, Hm, N, bq, bk, &L)) return 0;
+    if (!plan_layout(B, Hm, N, bq, bk, &L, q_row0, Nq)) return 0;
     return (size_t)L.total;
 }
 
-fm_status fm_tile_classify(fm_bounds m, int bq, int bk, void *plan, size_t plan_bytes, uint8_t *labels,
-                           int32_t *dev_status, fm_stream_t stream)
+size_t fm_plan_bytes(int B, int Hm, int N, int bq, int bk)
+{
+    return fm_plan_bytes_rows(B, Hm, N, 0, N, bq, bk);
+}
+
+fm_status fm_tile_classify_rows(fm_bounds m, int q_row0, int Nq, int bq, int bk, void *plan, size_t plan_bytes,
+                                uint8_t *labels, int32_t *dev_status, fm_stream_t stream)
 {
     PlanLayout L;
-    if (!plan_layout(m.B, m.Hm, m.N, bq, bk, &L)) return FM_ERR_INVALID_ARG;
+    if (!plan_layout(m.B, m.Hm, m.N, bq, bk, &L, q_row0, Nq)) return FM_ERR_INVALID_ARG;
     if (!plan || ((uintptr_t)plan & 255u) || plan_bytes < (size_t)L.total) return FM_ERR_WORKSPACE;
     if (!dev_status || ((uintptr_t)dev_status & 3u)) return FM_ERR_INVALID_ARG;
     if (!aligned16(m.lts) || !aligned16(m.lte) || !aligned16(m.uts) || !aligned16(m.ute))
@@ -199,7 +204,13 @@ fm_status fm_tile_classify(fm_bounds m, int bq, int bk, void *plan, size_t plan_
     if ((int64_t)m.B * m.Hm > 65535) return FM_ERR_UNSUPPORTED;
     const fm_status dv = check_device();
     if (dv != FM_OK) return dv;
-    return fm_classify_launch(m, bq, bk, plan, labels, dev_status, (cudaStream_t)stream);
+    return fm_classify_launch(m, q_row0, Nq, bq, bk, plan, labels, dev_status, (cudaStream_t)stream);
+}
+
+fm_status fm_tile_classify(fm_bounds m, int bq, int bk, void *plan, size_t plan_bytes, uint8_t *labels,
+                           int32_t *dev_status, fm_stream_t stream)
+{
+    return fm_tile_classify_rows(m, 0, m.N, bq, bk, plan, plan_bytes, labels, dev_status, stream);
 }
 
 size_t fm_fwd_workspace_bytes(int B, int H, int N, int d)
@@ -208,9 +219,9 @@ size_t fm_fwd_workspace_bytes(int B, int H, int N, int d)
     return 0;
 }
 
-fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, const void *plan, int B,
-                      int H, int N, int d, float scale, void *o, int o_dtype, float *lse, void *ws,
-                      size_t ws_bytes, int flags, int32_t *dev_status, fm_stream_t stream)
+fm_status fm_attn_fwd_rows(const void *q, const void *k, const void *v, fm_bounds m, const void *plan, int B,
+                           int H, int N, int q_row0, int Nq, int d, float scale, void *o, int o_dtype, float *lse,
+                           void *ws, size_t ws_bytes, int flags, int32_t *dev_status, fm_stream_t stream)
 {
     (void)ws; (void)ws_bytes;
     if (flags & ~FM_FLAG_PRECISE) return FM_ERR_INVALID_ARG;
@@ -223,11 +234,11 @@ fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, 
     if (o_dtype != FM_DT_BF16 && o_dtype != FM_DT_F32) return FM_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return FM_ERR_INVALID_ARG;
     PlanLayout L;
-    if (!plan_layout(B, m.Hm, N, 128, 128, &L)) return FM_ERR_INVALID_ARG;
+    if (!plan_layout(B, m.Hm, N, 128, 128, &L, q_row0, Nq)) return FM_ERR_INVALID_ARG;
     if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
     if ((st = check_device()) != FM_OK) return st;
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bf16(&tq, q, B * H, N, d, 128) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
+    if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 128) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
         !make_tmap_bf16(&tv, v, B * H, N, d, 128))
         return FM_ERR_CUDA;
     FwdArgs a;
@@ -235,9 +246,18 @@ fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, 
     a.plan = (const uint8_t *)plan; a.L = L;
     a.o = o; a.lse = lse; a.status = dev_status;
     a.B = B; a.H = H; a.Hm = m.Hm; a.N = N;
+    a.q_row0 = q_row0; a.Nq = Nq;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.o_f32 = o_dtype == FM_DT_F32;
     return fm_fwd_launch(tq, tk, tv, a, d, (flags & FM_FLAG_PRECISE) != 0, (cudaStream_t)stream);
+}
+
+fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, const void *plan, int B,
+                      int H, int N, int d, float scale, void *o, int o_dtype, float *lse, void *ws,
+                      size_t ws_bytes, int flags, int32_t *dev_status, fm_stream_t stream)
+{
+    return fm_attn_fwd_rows(q, k, v, m, plan, B, H, N, 0, N, d, scale, o, o_dtype, lse, ws, ws_bytes, flags,
+                            dev_status, stream);
 }
 
 size_t fm_bwd_workspace_bytes(int B, int H, int N, int d)
@@ -248,10 +268,11 @@ size_t fm_bwd_workspace_bytes(int B, int H, int N, int d)
     return (size_t)(acc + dvec);
 }
 
-fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o, int o_dtype,
-                      const float *lse, const void *dO, fm_bounds m, const void *plan, int B, int H,
-                      int N, int d, float scale, void *dq, void *dk, void *dv, int grad_dtype,
-                      int flags, void *ws, size_t ws_bytes, int32_t *dev_status, fm_stream_t stream)
+fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const void *o, int o_dtype,
+                           const float *lse, const void *dO, fm_bounds m, const void *plan, int B, int H,
+                           int N, int q_row0, int Nq, int d, float scale, void *dq, void *dk, void *dv,
+                           int grad_dtype, int flags, void *ws, size_t ws_bytes, int32_t *dev_status,
+                           fm_stream_t stream)
 {
     if (flags & ~FM_FLAG_PRECISE) return FM_ERR_INVALID_ARG;
     fm_status st = check_shapes(B, H, N, d);
@@ -265,19 +286,19 @@ fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o
         (grad_dtype != FM_DT_BF16 && grad_dtype != FM_DT_F32))
         return FM_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return FM_ERR_INVALID_ARG;
-    const size_t need = fm_bwd_workspace_bytes(B, H, N, d);
-    if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need) return FM_ERR_WORKSPACE;
     PlanLayout L;
-    if (!plan_layout(B, m.Hm, N, 128, 128, &L)) return FM_ERR_INVALID_ARG;
+    if (!plan_layout(B, m.Hm, N, 128, 128, &L, q_row0, Nq)) return FM_ERR_INVALID_ARG;
+    const size_t need = fm_bwd_workspace_bytes(B, H, Nq, d);
+    if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need) return FM_ERR_WORKSPACE;
     if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
     if ((st = check_device()) != FM_OK) return st;
     CUtensorMap tq, tk, tv, tdo;
     float *dq_acc = reinterpret_cast<float *>(ws);
-    if (!make_tmap_bf16(&tq, q, B * H, N, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
-        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, N, d, 64))
+    if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
+        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, 64))
         return FM_ERR_CUDA;
-    float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * N * d * 4));
-    const int64_t rows = (int64_t)B * H * N;
+    float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * Nq * d * 4));
+    const int64_t rows = (int64_t)B * H * Nq;
     cudaStream_t s = (cudaStream_t)stream;
     if ((st = fm_bwd_pre_launch(o, o_dtype == FM_DT_F32, dO, Dvec, dq_acc, rows, d, s)) != FM_OK) return st;
     BwdArgs a;
@@ -286,11 +307,21 @@ fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o
     a.lse = lse; a.Dvec = Dvec; a.dq_acc = dq_acc;
     a.dk = dk; a.dv = dv; a.status = dev_status;
     a.B = B; a.H = H; a.Hm = m.Hm; a.N = N;
+    a.q_row0 = q_row0; a.Nq = Nq;
     a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.g_f32 = grad_dtype == FM_DT_F32;
     if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
         return st;
     return fm_bwd_post_launch(dq_acc, dq, grad_dtype == FM_DT_F32, scale, rows * d, s);
+}
+
+fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o, int o_dtype,
+                      const float *lse, const void *dO, fm_bounds m, const void *plan, int B, int H,
+                      int N, int d, float scale, void *dq, void *dk, void *dv, int grad_dtype,
+                      int flags, void *ws, size_t ws_bytes, int32_t *dev_status, fm_stream_t stream)
+{
+    return fm_attn_bwd_rows(q, k, v, o, o_dtype, lse, dO, m, plan, B, H, N, 0, N, d, scale, dq, dk, dv,
+                            grad_dtype, flags, ws, ws_bytes, dev_status, stream);
 }
 
 struct fm_step_graph_st {

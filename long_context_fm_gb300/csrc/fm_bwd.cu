@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(736, 1)
     if (warp == 0) {
         const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(a.plan);
         bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
-                  ph->bq == 128 && ph->bk == 128;
+                  ph->bq == 128 && ph->bk == 128 && ph->q_row0 == L.q_row0 && ph->Nq == L.Nq;
         // KV tiles longest column list first (the plan's bucketed order); ok is warp-uniform.
         int ut = 0, uh = 0, ub = 0;
         const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
@@ -253,8 +253,9 @@ __global__ void __launch_bounds__(736, 1)
     __syncthreads();
     auto entry = [&](int t) { return t < S::kListCap ? sList[t] : glist[t]; };
     // Flat iteration over 64-row halves of the listed Q tiles.  Only the last
-    // Q tile can have a second half beyond N, and it is last in the list.
-    const int n_it = (cnt > 0 && (entry(cnt - 1) & kTileMask) * 128 + 64 >= N) ? 2 * cnt - 1 : 2 * cnt;
+    // Q tile can have a second half beyond the Q rows, and it is last in the list.
+    const int Nq = a.Nq;
+    const int n_it = (cnt > 0 && (entry(cnt - 1) & kTileMask) * 128 + 64 >= Nq) ? 2 * cnt - 1 : 2 * cnt;
     auto q0_of = [&](int it) { return (entry(it >> 1) & kTileMask) * 128 + (it & 1) * 64; };
 
     if (*ok_sh) {
@@ -275,16 +276,16 @@ __global__ void __launch_bounds__(736, 1)
                 const int q0 = q0_of(it);
                 const int st = it % NST;
                 // lse and D of the half's rows, loaded before the stage wait so
-                // the global latency overlaps it; rows beyond N get P = 0.
+                // the global latency overlaps it; rows beyond the Q rows get P = 0.
                 float lv[2], dv[2];
 #pragma unroll
                 for (int rr = 0; rr < 2; ++rr) {
                     const int qi = q0 + lane + rr * 32;
                     lv[rr] = INFINITY;
                     dv[rr] = 0.f;
-                    if (qi < N) {
-                        lv[rr] = a.lse[(int64_t)bh * N + qi];
-                        dv[rr] = a.Dvec[(int64_t)bh * N + qi];
+                    if (qi < Nq) {
+                        lv[rr] = a.lse[(int64_t)bh * Nq + qi];
+                        dv[rr] = a.Dvec[(int64_t)bh * Nq + qi];
                     }
                 }
                 if (it >= NST && !warp_wait(&bars[BB_QE0 + st], ((it / NST) - 1) & 1, abort, a.status)) break;
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(736, 1)
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1])), sc2, nl2[c / 2]), x0, x1);
                     float p0 = ex2(x0), p1 = ex2(x1);
                     if (pred) {
-                        const int qi = q0 + c0 + c;
+                        const int qi = a.q_row0 + q0 + c0 + c;   // row of the mask
                         const bool m0 = ((unsigned)(qi - lo0) < (unsigned)lolen) ||
                                         ((unsigned)(qi - up0) < (unsigned)uplen);
                         const bool m1 = ((unsigned)(qi + 1 - lo0) < (unsigned)lolen) ||
@@ -586,8 +587,8 @@ __global__ void __launch_bounds__(736, 1)
                 tc_fence_before();
                 mbar_arrive(&bars[BB_DQE0 + qb]);   // score buffer qb is free again
                 if (!has_cols) continue;
-                float *dst = a.dq_acc + ((int64_t)bh * N + q0) * D + dd;
-                const int lim = min(64, N - q0);       // rows beyond N: nothing to add
+                float *dst = a.dq_acc + ((int64_t)bh * Nq + q0) * D + dd;
+                const int lim = min(64, Nq - q0);      // rows beyond the Q rows: nothing to add
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
                     if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(128) classify_minmax_kernel(fm_bounds m, PlanL
         h->n_q = L.n_q; h->n_k = L.n_k; h->total = L.total;
         h->off_row_order = L.off_row_order; h->off_col_order = L.off_col_order;
         h->off_row_bstart = L.off_row_bstart; h->off_col_bstart = L.off_col_bstart;
+        h->q_row0 = L.q_row0; h->Nq = L.Nq;
         __threadfence();
         h->magic = kPlanMagic;
     }
@@ -98,7 +99,6 @@ __global__ void __launch_bounds__(128) classify_lists_kernel(PlanLayout L, uint8
                                                              uint8_t *labels_out)
 {
     const int s = blockIdx.y;
-    const int N = L.N;
     const int32_t *mm = reinterpret_cast<const int32_t *>(plan + L.off_minmax) + (int64_t)s * L.n_k * 8;
     __shared__ int warp_cnt[4];
     __shared__ int base_sh;
@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(128) classify_lists_kernel(PlanLayout L, uint8
         cnt = reinterpret_cast<int32_t *>(plan + L.off_row_cnt) + (int64_t)s * L.n_q + idx;
         lbl_row = plan + L.off_labels + ((int64_t)s * L.n_q + idx) * L.n_k;
         if (labels_out) lbl_out = labels_out + ((int64_t)s * L.n_q + idx) * L.n_k;
-        qb = idx * L.bq;
-        qe = min(qb + L.bq, N);
+        qb = L.q_row0 + idx * L.bq;
+        qe = min(qb + L.bq, L.q_row0 + L.Nq);
     } else {
         list = reinterpret_cast<int32_t *>(plan + L.off_col_list) + ((int64_t)s * L.n_k + idx) * L.n_q;
         cnt = reinterpret_cast<int32_t *>(plan + L.off_col_cnt) + (int64_t)s * L.n_k + idx;
@@ -135,8 +135,8 @@ __global__ void __launch_bounds__(128) classify_lists_kernel(PlanLayout L, uint8
                 lbl_row[c] = (uint8_t)lab;
                 if (lbl_out) lbl_out[c] = (uint8_t)lab;
             } else {
-                const int b0 = c * L.bq;
-                lab = tile_label(own, b0, min(b0 + L.bq, N));
+                const int b0 = L.q_row0 + c * L.bq;
+                lab = tile_label(own, b0, min(b0 + L.bq, L.q_row0 + L.Nq));
             }
         }
         const bool keep = c < n_other && lab != FM_TILE_SKIP;
@@ -216,11 +216,11 @@ __global__ void __launch_bounds__(kOrderThreads) classify_order_kernel(PlanLayou
 
 using namespace fm;
 
-fm_status fm_classify_launch(fm_bounds m, int bq, int bk, void *plan, uint8_t *labels,
+fm_status fm_classify_launch(fm_bounds m, int q_row0, int Nq, int bq, int bk, void *plan, uint8_t *labels,
                              int32_t *status, cudaStream_t stream)
 {
     PlanLayout L;
-    if (!plan_layout(m.B, m.Hm, m.N, bq, bk, &L)) return FM_ERR_INVALID_ARG;
+    if (!plan_layout(m.B, m.Hm, m.N, bq, bk, &L, q_row0, Nq)) return FM_ERR_INVALID_ARG;
     const int S = m.B * m.Hm;
     if (L.n_k > 65535 * 64 || S > 65535) return FM_ERR_UNSUPPORTED;
     {

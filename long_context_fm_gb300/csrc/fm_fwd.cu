@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(352, 1)
     if (warp == 0) {
         const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(a.plan);
         bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
-                  ph->bq == 128 && ph->bk == 128;
+                  ph->bq == 128 && ph->bk == 128 && ph->q_row0 == L.q_row0 && ph->Nq == L.Nq;
         // Q tiles longest row list first (the plan's bucketed order); ok is warp-uniform.
         int ut = 0, uh = 0, ub = 0;
         const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(352, 1)
             const int w = (warp < 6) ? 0 : 1;          // column half: KV columns [64 w, 64 w + 64)
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
-            const int i = qt * 128 + r;
+            const int li = qt * 128 + r;               // row of Q / O / lse
+            const int i = a.q_row0 + li;               // row of the mask
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const uint32_t tO = tmem + 384;
             constexpr int OC = D / 2;                  // O columns rescaled / stored by this warpgroup
@@ -432,8 +433,8 @@ __global__ void __launch_bounds__(352, 1)
                 tc_fence_after();
                 const float lt = sSum[r] + sSum[128 + r];
                 const float inv = (lt > 0.f) ? 1.f / lt : 0.f;
-                const bool row_in = i < N;
-                const int64_t row = (int64_t)bh * N + i;
+                const bool row_in = li < a.Nq;
+                const int64_t row = (int64_t)bh * a.Nq + li;
 #pragma unroll
                 for (int cc = 0; cc < OC / 32; ++cc) {
                     const int col = w * OC + cc * 32;

@@ -23,6 +23,7 @@ constexpr int32_t kTileMask = (1 << kLabelShift) - 1;
 // 256-byte boundary.
 struct PlanLayout {
     int32_t B, Hm, N, bq, bk, n_q, n_k;
+    int32_t q_row0, Nq;    // Q rows [q_row0, q_row0 + Nq) of the N x N mask (whole mask: 0, N)
     int64_t off_minmax;    // int32 [B*Hm][n_k][8]
     int64_t off_labels;    // uint8 [B*Hm][n_q][n_k]
     int64_t off_row_cnt;   // int32 [B*Hm][n_q]
@@ -54,21 +55,28 @@ struct PlanHeader {        // first 128 bytes of a plan, written by the classifi
     int32_t B, Hm, N, bq, bk, n_q, n_k;
     int64_t total;
     int64_t off_row_order, off_col_order, off_row_bstart, off_col_bstart;
-    int32_t pad[14];
+    int32_t q_row0, Nq;
+    int32_t pad[12];
 };
 static_assert(sizeof(PlanHeader) == 128, "plan header size");
 
 FM_HD int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
-FM_HD bool plan_layout(int B, int Hm, int N, int bq, int bk, PlanLayout *L)
+// Plan of the Q rows [q_row0, q_row0 + Nq) against all N key columns;
+// q_row0 is a multiple of bq, so local Q tile t covers global rows
+// [q_row0 + t bq, ...).  Nq < 0 means the whole mask (q_row0 = 0, Nq = N).
+FM_HD bool plan_layout(int B, int Hm, int N, int bq, int bk, PlanLayout *L, int q_row0 = 0, int Nq = -1)
 {
-    if (B <= 0 || Hm <= 0 || N <= 0) return false;
+    if (Nq < 0) { q_row0 = 0; Nq = N; }
+    if (B <= 0 || Hm <= 0 || N <= 0 || Nq <= 0 || q_row0 < 0) return false;
     if (!((bq == 64 || bq == 128) && (bk == 64 || bk == 128))) return false;
-    const int64_t n_q = (N + bq - 1) / bq, n_k = (N + bk - 1) / bk;
+    if (q_row0 % bq != 0 || (int64_t)q_row0 + Nq > N) return false;
+    const int64_t n_q = (Nq + bq - 1) / bq, n_k = (N + bk - 1) / bk;
     if (n_q >= kTileMask || n_k >= kTileMask) return false;
     const int64_t S = (int64_t)B * Hm;
     if (S * (n_q > n_k ? n_q : n_k) >= ((int64_t)1 << 31)) return false;   // order entries are int32
     L->B = B; L->Hm = Hm; L->N = N; L->bq = bq; L->bk = bk;
+    L->q_row0 = q_row0; L->Nq = Nq;
     L->n_q = (int32_t)n_q; L->n_k = (int32_t)n_k;
     int64_t off = 256;
     L->off_minmax = off;   off = align256(off + S * n_k * 8 * 4);
@@ -134,6 +142,7 @@ struct FwdArgs {
     float *lse;
     int32_t *status;
     int B, H, Hm, N;
+    int q_row0, Nq;       // Q, O, lse hold rows [q_row0, q_row0 + Nq) of the mask
     float scale_log2;     // softmax scale * log2(e)
     int o_f32;
 };
@@ -149,6 +158,7 @@ struct BwdArgs {
     void *dk, *dv;
     int32_t *status;
     int B, H, Hm, N;
+    int q_row0, Nq;       // Q, dO, lse, D, dQ hold rows [q_row0, q_row0 + Nq); K, V, dK, dV all N
     float scale, scale_log2;
     int g_f32;
 };

@@ -29,7 +29,8 @@ KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "b
 EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_mask_from_row_intervals",
             "fm_plan_bytes", "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
             "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
-            "fm_attn_bwd_noalloc", "fm_step_graph_create", "fm_step_graph_launch", "fm_step_graph_destroy"]
+            "fm_attn_bwd_noalloc", "fm_step_graph_create", "fm_step_graph_launch", "fm_step_graph_destroy",
+            "fm_plan_bytes_rows", "fm_tile_classify_rows", "fm_attn_fwd_rows", "fm_attn_bwd_rows"]
 # Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -84,6 +85,13 @@ _lib.fm_profile_begin.argtypes = []
 _lib.fm_profile_end.restype = _I
 _lib.fm_profile_end.argtypes = [_P, _I]
 _lib.fm_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _P, _P]
+_lib.fm_plan_bytes_rows.restype = _SZ
+_lib.fm_plan_bytes_rows.argtypes = [_I, _I, _I, _I, _I, _I, _I]
+_lib.fm_tile_classify_rows.argtypes = [Bounds, _I, _I, _I, _I, _P, _SZ, _P, _P, _P]
+_lib.fm_attn_fwd_rows.argtypes = [_P, _P, _P, Bounds, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P, _SZ, _I,
+                                  _P, _P]
+_lib.fm_attn_bwd_rows.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                  _P, _I, _I, _P, _SZ, _P, _P]
 _lib.fm_step_graph_create.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(ctypes.c_void_p)]
 _lib.fm_step_graph_launch.argtypes = [_P, _P]
 _lib.fm_step_graph_destroy.argtypes = [_P]
@@ -273,6 +281,61 @@ def fm_selftest_wait_timeout(limit_cycles, dev_status, stream=None):
 # Convenience layer: allocates the caller-owned buffers with torch and calls
 # the entry points above.
 # ---------------------------------------------------------------------------
+def fm_plan_bytes_rows(B, Hm, N, q_row0, Nq, bq=128, bk=128) -> int:
+    return int(_lib.fm_plan_bytes_rows(B, Hm, N, q_row0, Nq, bq, bk))
+
+
+def fm_tile_classify_rows(bounds: Bounds, q_row0, Nq, plan, dev_status, bq=128, bk=128, labels=None, stream=None):
+    _dev(plan, torch.uint8, "plan")
+    _dev(dev_status, torch.int32, "dev_status")
+    if labels is not None:
+        _dev(labels, torch.uint8, "labels")
+    code = _lib.fm_tile_classify_rows(bounds, int(q_row0), int(Nq), bq, bk, _ptr(plan), plan.numel(),
+                                      _ptr(labels), _ptr(dev_status), _stream(stream))
+    _check(code, "fm_tile_classify_rows")
+
+
+def fm_attn_fwd_rows(q, k, v, bounds: Bounds, plan, q_row0, scale, o, lse, dev_status, stream=None, flags=0):
+    """Q rows [q_row0, q_row0 + Nq) (q: [B, H, Nq, d]) against all N keys (k, v: [B, H, N, d])."""
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, torch.bfloat16, n)
+    B, H, Nq, d = q.shape
+    N = k.shape[2]
+    if k.shape != (B, H, N, d) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("q, o: [B, H, Nq, d]; k, v: [B, H, N, d]")
+    _dev(o, o.dtype, "o")
+    _dev(lse, torch.float32, "lse")
+    _dev(plan, torch.uint8, "plan")
+    _dev(dev_status, torch.int32, "dev_status")
+    code = _lib.fm_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), bounds, _ptr(plan), B, H, N, int(q_row0), Nq, d,
+                                 float(scale), _ptr(o), _dt(o), _ptr(lse), None, 0, int(flags), _ptr(dev_status),
+                                 _stream(stream))
+    _check(code, "fm_attn_fwd_rows")
+
+
+def fm_attn_bwd_rows(q, k, v, o, lse, dO, bounds: Bounds, plan, q_row0, scale, dq, dk, dv, ws, dev_status,
+                     stream=None, flags=0):
+    """dQ of the window's rows; dK, dV receive the window's contribution (all N rows)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("dO", dO)):
+        _dev(t, torch.bfloat16, n)
+    B, H, Nq, d = q.shape
+    N = k.shape[2]
+    for n, t, shp in (("o", o, q.shape), ("dq", dq, q.shape), ("dO", dO, q.shape), ("dk", dk, k.shape),
+                      ("dv", dv, k.shape)):
+        _dev(t, t.dtype, n)
+        if t.shape != shp:
+            raise ValueError(f"{n} has the wrong shape")
+    if not (dq.dtype == dk.dtype == dv.dtype):
+        raise TypeError("dq, dk, dv must share one dtype")
+    _dev(lse, torch.float32, "lse")
+    _dev(ws, torch.uint8, "ws")
+    code = _lib.fm_attn_bwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(lse), _ptr(dO), bounds,
+                                 _ptr(plan), B, H, N, int(q_row0), Nq, d, float(scale), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), _dt(dq), int(flags), _ptr(ws), ws.numel(), _ptr(dev_status),
+                                 _stream(stream))
+    _check(code, "fm_attn_bwd_rows")
+
+
 def fm_step_graph_create(q, k, v, dO, bounds: Bounds, plan, scale, o, lse, dev_status, dq=None, dk=None,
                          dv=None, ws=None, flags=0):
     """Capture classify + forward (+ backward when dO is given) for these
