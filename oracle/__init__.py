@@ -223,3 +223,76 @@ def tile_labels_all(mask, bq=128, bk=128, exact=False) -> np.ndarray:
     B, Hm, _ = mask["lts"].shape
     return np.stack([np.stack([tile_labels(*_bounds_of(mask, b, hm), bq, bk, exact)
                                for hm in range(Hm)]) for b in range(B)])
+
+
+# ---- FP8 (e4m3) --------------------------------------------------------------
+# The e4m3 format of the FP8 path (sign, 4 exponent bits with bias 7, 3 mantissa
+# bits; subnormals below 2^-6 in steps of 2^-9; no infinities; 0x7F / 0xFF are
+# NaN, so the largest finite value is 448 = 0x7E).  Per-tensor scaling (blog
+# "FlashMask技术" §4.2, FP8 compute mode on TMA/tensor-core hardware; the scale
+# rule is the plainest one): descale = amax / 448 in fp32 (1 when amax = 0),
+# code = e4m3(x / descale), the division in fp32, rounding to nearest even,
+# saturating at +-448.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values (float64) of e4m3 codes (uint8); NaN codes give NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round finite values to the nearest e4m3 code (ties to even), saturating."""
+    y = np.asarray(x, dtype=np.float64)
+    a = np.abs(y)
+    sign = np.where(np.signbit(y), 0x80, 0).astype(np.int64)
+    a = np.minimum(a, E4M3_MAX)
+    # exponent of the binade holding a (normal range), clamped at the subnormal one
+    E = np.floor(np.log2(np.where(a > 0, a, 1.0))).astype(np.int64)
+    E = np.clip(E, -6, 8)
+    step = 2.0 ** (E - 3)                     # spacing of the 8 mantissa steps of the binade
+    q = np.rint(a / step)                     # nearest multiple of the spacing, ties to even
+    # q in [8, 16] for normal binades (16: carried into the next binade), [0, 8] for E = -6
+    val = q * step
+    val = np.minimum(val, E4M3_MAX)
+    code = np.zeros(a.shape, np.int64)
+    nz = val > 0
+    Ev = np.floor(np.log2(np.where(nz, val, 1.0))).astype(np.int64)
+    sub = nz & (Ev < -6)
+    code = np.where(sub, np.rint(val / 2.0 ** -9).astype(np.int64), code)
+    nrm = nz & ~sub
+    mant = np.rint((val / 2.0 ** Ev - 1.0) * 8).astype(np.int64)
+    code = np.where(nrm, ((Ev + 7) << 3) | mant, code)
+    return (code | sign).astype(np.uint8)
+
+
+def quantize_e4m3(x, transpose=False):
+    """Per-tensor e4m3 quantization of a [B, H, N, d] tensor: (codes uint8, descale
+    float32).  transpose=True returns the codes as [B, H, d, N]."""
+    xf = _f32(x)
+    amax = np.float32(np.max(np.abs(xf))) if xf.size else np.float32(0)
+    descale = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+    y = (xf / descale).astype(np.float32)               # fp32 division, as the device does it
+    codes = e4m3_encode(y)
+    if transpose:
+        codes = np.ascontiguousarray(np.swapaxes(codes, 2, 3))
+    return codes, descale
+
+
+def forward_fp8(q8, k8, vt8, descale, mask, scale, rows=None):
+    """Attention on e4m3 inputs (q8, k8: [B, H, N, d] codes; vt8: [B, H, d, N]),
+    exactly: s_ij = scale * dq * dk * sum_c q_ic k_jc on the decoded values,
+    O = dv * sum_j P_ij v_j.  descale = (dq, dk, dv)."""
+    dq, dk, dv = (float(x) for x in descale)
+    qv = e4m3_decode(q8).astype(np.float32)             # e4m3 values are exact in fp32
+    kv = e4m3_decode(k8).astype(np.float32)
+    vv = np.ascontiguousarray(np.swapaxes(e4m3_decode(vt8), 2, 3)).astype(np.float32)
+    O, L = forward(qv, kv, vv, mask, scale * dq * dk, rows=rows)
+    return O * dv, L

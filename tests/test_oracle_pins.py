@@ -415,3 +415,66 @@ def test_labels_sound_with_one_random_range_per_column(seed, which):
         ex = oracle.tile_labels(*b, bq, bk, exact=True)
         assert np.all(ex[lbl == 0] == 0) and np.all(ex[lbl == 1] == 1)
         assert (lbl == 1).any()
+
+
+# ---- e4m3 (FP8 forward) --------------------------------------------------------
+def test_e4m3_codes_of_the_format_definition():
+    """Codes fixed by the format: sign | 4-bit exponent (bias 7) | 3-bit mantissa,
+    subnormals in steps of 2^-9, largest finite 448, ties to even, saturation."""
+    cases = [(1.0, 0x38), (2.0, 0x40), (0.5, 0x30), (1.125, 0x39), (448.0, 0x7E), (-448.0, 0xFE),
+             (500.0, 0x7E), (1e9, 0x7E), (-1e9, 0xFE), (2.0 ** -6, 0x08), (2.0 ** -9, 0x01),
+             (7 * 2.0 ** -9, 0x07), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (1.0625, 0x38),
+             (1.1875, 0x3A), (240.0, 0x77), (256.0, 0x78), (0.0, 0x00), (-0.0, 0x80)]
+    for x, c in cases:
+        assert int(oracle.e4m3_encode(np.array([x]))[0]) == c, x
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    vals = oracle.e4m3_decode(codes)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+    pos = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0) and pos[-1] == 448.0 and pos[1] == 2.0 ** -9
+    assert np.isnan(oracle.e4m3_decode(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_encode_matches_exhaustive_nearest_search():
+    """Nearest grid value by brute force over the 127 non-negative codes, ties to
+    the even code (an even mantissa), saturating at 448."""
+    rng = np.random.default_rng(8)
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (grid[1:] + grid[:-1]) / 2
+    x = np.concatenate([np.exp2(rng.uniform(-12, 9.5, 4000)), mids, grid, [470.0, 455.0]])
+    x = np.concatenate([x, -x[:500]])
+    got = oracle.e4m3_encode(x)
+    a = np.minimum(np.abs(x), 448.0)
+    dist = np.abs(a[:, None] - grid[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist <= best                                   # one or two nearest codes
+    code = np.array([np.flatnonzero(row)[0] if row.sum() == 1 else
+                     [c for c in np.flatnonzero(row) if c % 2 == 0][0] for row in cand])
+    want = (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_quantize_e4m3_scale_and_reduction_to_the_exact_path():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 2, 40, 16)).astype(np.float32)
+    codes, ds = oracle.quantize_e4m3(x)
+    assert ds == np.float32(np.abs(x).max() / np.float32(448.0))
+    i = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert codes[i] & 0x7F == 0x7E                        # the largest magnitude maps to +-448
+    assert np.abs(oracle.e4m3_decode(codes) * ds - x).max() <= np.abs(x).max() / 448 * 16   # half a top-binade step
+    # values already on the e4m3 grid with amax 448 are kept exactly (descale 1), so
+    # the FP8 path reduces to the plain one
+    g = oracle.e4m3_decode(rng.integers(0, 0x7F, size=(1, 2, 40, 16)).astype(np.uint8))
+    g *= np.where(rng.random(g.shape) < 0.5, -1.0, 1.0)
+    g.flat[0] = 448.0
+    q8, dq = oracle.quantize_e4m3(g)
+    assert dq == 1.0 and np.array_equal(oracle.e4m3_decode(q8), g)
+    k8, dk = oracle.quantize_e4m3(g[:, :, ::-1].copy())
+    vt8, dv = oracle.quantize_e4m3(g, transpose=True)
+    assert vt8.shape == (1, 2, 16, 40)
+    wl = W.Workload("c", 1, 1, 40, 16, "causal")
+    m = _mask_np(wl)
+    O8, L8 = oracle.forward_fp8(q8, k8, vt8, (dq, dk, dv), m, 0.1)
+    O, L = oracle.forward(g.astype(np.float32), g[:, :, ::-1].astype(np.float32), g.astype(np.float32), m, 0.1)
+    np.testing.assert_allclose(O8, O, rtol=0, atol=0)
+    np.testing.assert_allclose(L8, L, rtol=0, atol=0)
