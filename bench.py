@@ -11,7 +11,8 @@ row-form mask conversion on the host, host-to-device copies of Q, K, V, dO
 and the bounds, the device work, and device-to-host copies of O, lse, dQ,
 dK, dV, all inside the timed region.  `graph` times the same step captured
 once into a CUDA graph (fm_step_graph_create) and replayed, one launch per
-step.
+step.  `fp8_fwd` times the forward on e4m3 inputs (fm_attn_fwd_fp8) and the
+quantization of Q, K, V beside it.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fm|reference]
 Under torchrun every rank runs the whole workload on its own GPU (independent
@@ -225,6 +226,37 @@ def run_fm(args, rank, world, local_rank):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in graph replay")
 
+    # ---- FP8 forward: e4m3 Q, K, V^T (per-tensor scales); the forward timed
+    # alone, and one quantization of Q, K, V timed beside it
+    fp8 = None
+    if d == 128 and N % 16 == 0:
+        q8, dq8 = fm.fm_quantize_fp8(q, stream=stream)
+        k8, dk8 = fm.fm_quantize_fp8(k, stream=stream)
+        vt8, dv8 = fm.fm_quantize_fp8(v, transpose=True, stream=stream)
+        descale = torch.cat([dq8, dk8, dv8])
+        o8 = torch.empty_like(o)
+
+        def fwd8():
+            fm.fm_attn_fwd_fp8(q8, k8, vt8, descale, bounds, plan, scale, o8, lse, status, stream=stream)
+
+        for _ in range(max(args.warmup, 2)):
+            fwd8()
+        torch.cuda.synchronize(dev)
+        f0, f1, f2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        f0.record(stream)
+        for _ in range(args.steps):
+            fwd8()
+        f1.record(stream)
+        for _ in range(args.steps):
+            fm.fm_quantize_fp8(q, out=q8, descale=dq8, stream=stream)
+            fm.fm_quantize_fp8(k, out=k8, descale=dk8, stream=stream)
+            fm.fm_quantize_fp8(v, transpose=True, out=vt8, descale=dv8, stream=stream)
+        f2.record(stream)
+        torch.cuda.synchronize(dev)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in the FP8 forward")
+        fp8 = (f0.elapsed_time(f1) / args.steps, f1.elapsed_time(f2) / args.steps)
+
     # ---- end to end through the C ABI from pinned host buffers
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dO))
     rows = m["rows"]
@@ -266,7 +298,7 @@ def run_fm(args, rank, world, local_rank):
     ms_step, e2e_s, graph_ms = max_over_ranks([ms_step, e2e_s, graph_ms], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
                 avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h,
-                graph_ms=graph_ms)
+                graph_ms=graph_ms, fp8=fp8)
 
 
 def mask_description(wl):
@@ -391,6 +423,10 @@ def main():
                          "peak": peak_sus, "unit": "TFLOP/s", "frac": bwd_tflops / peak_sus,
                          "traffic": traffic, "peak_source": f"{src} bf16 sustained"},
             "gpu_launches": r["launches"],
+            "fp8_fwd": None if r["fp8"] is None else {
+                "ms": r["fp8"][0], "value": world * r["fwd_flops"] / (r["fp8"][0] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "quantize_qkv_ms": r["fp8"][1],
+                "note": "e4m3 Q, K, V^T with per-tensor scales, P rounded to e4m3; forward alone, same FLOPs"},
             "graph": {"ms_per_step": r["graph_ms"], "value": world * step_flops / (r["graph_ms"] * 1e-3) / 1e12,
                       "unit": "TFLOP/s", "launches_per_step": 1,
                       "note": "the same step captured once (fm_step_graph_create) and replayed"},

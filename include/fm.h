@@ -259,6 +259,29 @@ FM_API fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, c
                            void *ws, size_t ws_bytes, int32_t *dev_status, fm_stream_t stream);
 
 /*
+ * FP8 forward — DEVICE, async.  Passage: blog "FlashMask技术" §4.2 (the
+ * H100 path computes in FP8); per-tensor scaling is the plainest reading.
+ * fm_quantize_fp8: e4m3 codes of a bf16 [B, H, N, d] tensor with one scale,
+ *   descale = amax / 448 (1 if amax = 0), code = e4m3(x / descale) (fp32
+ *   division, round to nearest even, saturating at +-448; inputs finite).
+ *   transpose = 0: x8 is [B, H, N, d]; 1: x8 is [B, H, d, N] (N a multiple
+ *   of 16, else FM_ERR_UNSUPPORTED) — the layout fm_attn_fwd_fp8 wants for V.
+ *   descale: device float, written.  d = 64 or 128.
+ * fm_attn_fwd_fp8: fm_attn_fwd (whole mask, standard mode, d = 128) on e4m3
+ *   q8, k8 [B, H, N, d] and vt8 [B, H, d, N] with descale = device float[3]
+ *   (Q, K, V): S = scale * dq * dk * Q8 K8^T, P rounded to e4m3 for the P V
+ *   product (P <= 256 under the lazy rescale), O = dv * (P V) / sum P.  N a
+ *   multiple of 16; d != 128 -> FM_ERR_UNSUPPORTED.  Same plan, bounds and
+ *   outputs as fm_attn_fwd.
+ */
+FM_API fm_status fm_quantize_fp8(const void *x, int B, int H, int N, int d, int transpose, uint8_t *x8,
+                          float *descale, fm_stream_t stream);
+FM_API fm_status fm_attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *vt8,
+                          const float *descale, fm_bounds m, const void *plan, int B, int H, int N,
+                          int d, float scale, void *o, int o_dtype, float *lse, int32_t *dev_status,
+                          fm_stream_t stream);
+
+/*
  * Step graphs — create / destroy HOST, synchronous; launch DEVICE, async.
  * One step of the path (fm_tile_classify, fm_attn_fwd and, when dO is given,
  * fm_attn_bwd; 128 x 128 tiles) captured once into a CUDA graph for a fixed
@@ -306,7 +329,8 @@ FM_API fm_status fm_step_graph_destroy(fm_step_graph graph);
  * stops recording.  Returns the number of records written, or -1 on error.
  */
 enum { FM_K_CLASSIFY_MINMAX = 0, FM_K_CLASSIFY_LISTS = 1, FM_K_FWD = 2, FM_K_BWD_PRE = 3,
-       FM_K_BWD = 4, FM_K_BWD_POST = 5, FM_K_CLASSIFY_ORDER = 6, FM_K_COUNT = 7 };
+       FM_K_BWD = 4, FM_K_BWD_POST = 5, FM_K_CLASSIFY_ORDER = 6, FM_K_FP8_AMAX = 7,
+       FM_K_FP8_CONVERT = 8, FM_K_COUNT = 9 };
 typedef struct {
     int32_t kernel;
     float ms;

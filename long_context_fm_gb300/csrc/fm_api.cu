@@ -24,6 +24,9 @@ fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dou
 fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,
                              cudaStream_t stream);
 fm_status fm_fwd_prepare(int d, bool precise);
+fm_status fm_fwd_prepare_fp8();
+fm_status fm_fwd_launch_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
+                            const FwdArgs &a, cudaStream_t stream);
 fm_status fm_bwd_prepare(int d, bool precise);
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const FwdArgs &a, int d, bool precise, cudaStream_t stream);
@@ -33,7 +36,7 @@ fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const
 
 namespace {
 
-constexpr int kAbiVersion = 5;
+constexpr int kAbiVersion = 6;
 
 bool aligned16(const void *p) { return p && ((uintptr_t)p & 15u) == 0; }
 
@@ -65,6 +68,22 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, int BH, int N, int d, in
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                           box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// uint8 [BH, rows, cols] viewed as 3-D (cols, rows, BH); box = 128 columns x
+// `box_rows` rows, 128-byte swizzle (one box spans a 128-byte row), zero fill.
+bool make_tmap_u8(CUtensorMap *map, const void *base, int BH, int rows, int cols, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)rows * cols};
+    const cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -249,7 +268,42 @@ fm_status fm_attn_fwd_rows(const void *q, const void *k, const void *v, fm_bound
     a.q_row0 = q_row0; a.Nq = Nq;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.o_f32 = o_dtype == FM_DT_F32;
+    a.descale = nullptr;
     return fm_fwd_launch(tq, tk, tv, a, d, (flags & FM_FLAG_PRECISE) != 0, (cudaStream_t)stream);
+}
+
+fm_status fm_attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *vt8, const float *descale,
+                          fm_bounds m, const void *plan, int B, int H, int N, int d, float scale, void *o,
+                          int o_dtype, float *lse, int32_t *dev_status, fm_stream_t stream)
+{
+    fm_status st = check_shapes(B, H, N, d);
+    if (st != FM_OK) return st;
+    if (d != 128 || N % 16 != 0) return FM_ERR_UNSUPPORTED;
+    if ((st = check_bounds(m, B, H, N)) != FM_OK) return st;
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned16(lse))
+        return FM_ERR_INVALID_ARG;
+    if (!descale || ((uintptr_t)descale & 3u)) return FM_ERR_INVALID_ARG;
+    if (!dev_status || ((uintptr_t)dev_status & 3u)) return FM_ERR_INVALID_ARG;
+    if (o_dtype != FM_DT_BF16 && o_dtype != FM_DT_F32) return FM_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FM_ERR_INVALID_ARG;
+    PlanLayout L;
+    if (!plan_layout(B, m.Hm, N, 128, 128, &L)) return FM_ERR_INVALID_ARG;
+    if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
+    if ((st = check_device()) != FM_OK) return st;
+    CUtensorMap tq, tk, tvt;
+    if (!make_tmap_u8(&tq, q8, B * H, N, d, 128) || !make_tmap_u8(&tk, k8, B * H, N, d, 128) ||
+        !make_tmap_u8(&tvt, vt8, B * H, d, N, d))
+        return FM_ERR_CUDA;
+    FwdArgs a;
+    a.lts = m.lts; a.lte = m.lte; a.uts = m.uts; a.ute = m.ute;
+    a.plan = (const uint8_t *)plan; a.L = L;
+    a.o = o; a.lse = lse; a.status = dev_status;
+    a.B = B; a.H = H; a.Hm = m.Hm; a.N = N;
+    a.q_row0 = 0; a.Nq = N;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.o_f32 = o_dtype == FM_DT_F32;
+    a.descale = descale;
+    return fm_fwd_launch_fp8(tq, tk, tvt, a, (cudaStream_t)stream);
 }
 
 fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, const void *plan, int B,

@@ -41,10 +41,10 @@
 
 namespace fm {
 
-template <int D>
+template <int D, bool FP8 = false>
 struct FwdSmem {
-    static constexpr int kBox = 128 * 128;        // one 64-column, 128-row bf16 box
-    static constexpr int kTile = 128 * D * 2;     // one Q, K or V tile
+    static constexpr int kBox = 128 * 128;        // one 128-byte wide, 128-row box (64 bf16 or 128 e4m3 columns)
+    static constexpr int kTile = 128 * D * (FP8 ? 1 : 2);   // one Q, K or V tile
     static constexpr int kKStages = 3, kVStages = 2;
     static constexpr int kQ = 0;
     static constexpr int kK = kTile;                           // [kKStages]
@@ -75,13 +75,16 @@ enum {
 constexpr int kSB = 3;              // score buffers in TMEM
 constexpr int kSoftmaxBar = 1;      // named barrier of the two softmax warpgroups (256 threads)
 
-template <int D, bool PRECISE>
+template <int D, bool PRECISE, bool FP8>
 __global__ void __launch_bounds__(352, 1)
     fm_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a)
 {
-    using S = FwdSmem<D>;
-    constexpr int NBOX = D / 64;
+    static_assert(!(PRECISE && FP8), "the FP8 path has no precise mode");
+    static_assert(!FP8 || D == 128, "the FP8 path is built for d = 128");
+    using S = FwdSmem<D, FP8>;
+    constexpr int BOXW = FP8 ? 128 : 64;          // elements per 128-byte box row
+    constexpr int NBOX = D / BOXW;
     constexpr int KS = S::kKStages, VS = S::kVStages;
     // The kernel has no static shared memory, so the dynamic window starts on
     // a 1024-byte boundary (checked below).  Pointers stay derived from the
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(352, 1)
                 mbar_arrive_expect_tx(&bars[FB_Q], S::kTile);
 #pragma unroll
                 for (int x = 0; x < NBOX; ++x)
-                    tma_load_3d(smem + S::kQ + x * S::kBox, &tq, &bars[FB_Q], x * 64, qt * 128, bh);
+                    tma_load_3d(smem + S::kQ + x * S::kBox, &tq, &bars[FB_Q], x * BOXW, qt * 128, bh);
             }
             int nk = 0;   // K loads issued
             for (int t = 0; t < n; ++t) {
@@ -186,7 +189,7 @@ __global__ void __launch_bounds__(352, 1)
                     mbar_arrive_expect_tx(&bars[FB_KF0 + ks], S::kTile);
 #pragma unroll
                     for (int x = 0; x < NBOX; ++x)
-                        tma_load_3d(smem + S::kK + ks * S::kTile + x * S::kBox, &tk, &bars[FB_KF0 + ks], x * 64, kb, bh);
+                        tma_load_3d(smem + S::kK + ks * S::kTile + x * S::kBox, &tk, &bars[FB_KF0 + ks], x * BOXW, kb, bh);
                 }
                 ++nk;
             }
@@ -227,8 +230,11 @@ __global__ void __launch_bounds__(352, 1)
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bars[FB_VF0 + vs], S::kTile);
 #pragma unroll
-                    for (int x = 0; x < NBOX; ++x)
-                        tma_load_3d(smem + S::kV + vs * S::kTile + x * S::kBox, &tv, &bars[FB_VF0 + vs], x * 64, kb, bh);
+                    if (FP8)   // V^T tile: d rows x 128 key columns, [B*H][d][N] e4m3
+                        tma_load_3d(smem + S::kV + vs * S::kTile, &tv, &bars[FB_VF0 + vs], kb, 0, bh);
+                    else
+                        for (int x = 0; x < NBOX; ++x)
+                            tma_load_3d(smem + S::kV + vs * S::kTile + x * S::kBox, &tv, &bars[FB_VF0 + vs], x * 64, kb, bh);
                 }
                 ++nv;
                 if (pred) {
@@ -264,10 +270,16 @@ __global__ void __launch_bounds__(352, 1)
                     tc_fence_after();
                     const uint64_t dK = sdesc_sw128(smem_u32(smem + S::kK + ks * S::kTile), 16, 1024);
                     const uint32_t tS = tmem + (t % kSB) * 128;
+                    if (FP8) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * S::kBox + (kk & 3) * 32;
-                        mma_ss(tS, sdesc_add(dQ, off), sdesc_add(dK, off), idS, kk > 0);
+                        for (int kk = 0; kk < D / 32; ++kk)   // K = 32 e4m3 = 32 bytes per instruction
+                            mma_ss_e4m3(tS, sdesc_add(dQ, kk * 32), sdesc_add(dK, kk * 32), idesc_e4m3(128, 128), kk > 0);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * S::kBox + (kk & 3) * 32;
+                            mma_ss(tS, sdesc_add(dQ, off), sdesc_add(dK, off), idS, kk > 0);
+                        }
                     }
                     tc_commit(&bars[FB_S0 + t % kSB]);
                     tc_commit(&bars[FB_KE0 + ks]);
@@ -283,14 +295,22 @@ __global__ void __launch_bounds__(352, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t dV = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), S::kBox, 1024);
                     const uint32_t tP = tmem + (t % kSB) * 128;
+                    if (FP8) {
+                        // B = V^T, K-major (d rows of 128 key bytes); A = P, 4 e4m3 per column
+                        const uint64_t dVt = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), 16, 1024);
 #pragma unroll
-                    for (int part = 0; part < NPART; ++part)   // P_hi V (+ P_lo V)
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts_e4m3(tO, tP + kk * 8, sdesc_add(dVt, kk * 32), idesc_e4m3(128, D), (t > 0 || kk > 0));
+                    } else {
+                        const uint64_t dV = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), S::kBox, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tO, tP + part * 64 + kk * 8, sdesc_add(dV, kk * 2048), idO,
-                                   (t > 0 || part > 0 || kk > 0));
+                        for (int part = 0; part < NPART; ++part)   // P_hi V (+ P_lo V)
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_ts(tO, tP + part * 64 + kk * 8, sdesc_add(dV, kk * 2048), idO,
+                                       (t > 0 || part > 0 || kk > 0));
+                    }
                     tc_commit(&bars[FB_O0 + t % kSB]);
                     tc_commit(&bars[FB_VE0 + vs]);
                 }
@@ -311,6 +331,8 @@ __global__ void __launch_bounds__(352, 1)
             const uint32_t tO = tmem + 384;
             constexpr int OC = D / 2;                  // O columns rescaled / stored by this warpgroup
             float m = -INFINITY, l = 0.f;
+            // softmax scale * log2(e), with the Q and K descales on the FP8 path
+            const float sl2 = FP8 ? a.scale_log2 * a.descale[0] * a.descale[1] : a.scale_log2;
             // `live` turns false (for the whole warp) when a wait gives up after an
             // abort; the warp then skips its work but still reaches every named
             // barrier of the loop, so the other warpgroup is never left waiting.
@@ -362,7 +384,7 @@ __global__ void __launch_bounds__(352, 1)
                 named_bar_sync(kSoftmaxBar, 256);
                 tc_fence_after();
                 if (!live) continue;
-                const float mx = fmaxf(mxl, sMax[(slot * 2 + (1 - w)) * 128 + r]) * a.scale_log2;   // -inf stays -inf
+                const float mx = fmaxf(mxl, sMax[(slot * 2 + (1 - w)) * 128 + r]) * sl2;   // -inf stays -inf
                 float m_new = m, alpha = 1.f;
                 if (mx > m + 8.f) {
                     m_new = mx;
@@ -394,7 +416,8 @@ __global__ void __launch_bounds__(352, 1)
                 // relative at most, far inside the tolerance, and summing the
                 // rounded values instead costs 1.5 instructions per element on
                 // the critical chain).  Column pairs in packed fp32.
-                const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nm2 = f2_pack(-m_use, -m_use);
+                const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
+                uint32_t f8[16];          // FP8: the warpgroup's 64 P values, 4 e4m3 per column
                 uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -406,14 +429,20 @@ __global__ void __launch_bounds__(352, 1)
                         const float p0 = ex2(x0), p1 = ex2(x1);
                         sum2 = f2_add(sum2, f2_pack(p0, p1));
                         hi[cc] = pack_bf16x2(p0, p1);
+                        if (FP8) {
+                            const uint32_t e2 = pack_e4m3x2(p0, p1);     // columns 2 cc, 2 cc + 1
+                            if (cc & 1) f8[hh * 8 + (cc >> 1)] |= e2 << 16;
+                            else f8[hh * 8 + (cc >> 1)] = e2;
+                        }
                         if (PRECISE) {
                             lo[cc] = pack_bf16x2(p0 - __uint_as_float(hi[cc] << 16),
                                                  p1 - __uint_as_float(hi[cc] & 0xffff0000u));
                         }
                     }
-                    tmem_st16(tS + lane_off + w * 32 + hh * 16, hi);
+                    if (!FP8) tmem_st16(tS + lane_off + w * 32 + hh * 16, hi);
                     if (PRECISE) tmem_st16(tS + lane_off + 64 + w * 32 + hh * 16, lo);
                 }
+                if (FP8) tmem_st16(tS + lane_off + w * 16, f8);   // columns [16 w, 16 w + 16)
                 float s0, s1;
                 f2_unpack(sum2, s0, s1);
                 l = l * alpha + (s0 + s1);
@@ -432,7 +461,7 @@ __global__ void __launch_bounds__(352, 1)
             if (live) {
                 tc_fence_after();
                 const float lt = sSum[r] + sSum[128 + r];
-                const float inv = (lt > 0.f) ? 1.f / lt : 0.f;
+                const float inv = (lt > 0.f) ? (FP8 ? a.descale[2] : 1.f) / lt : 0.f;
                 const bool row_in = li < a.Nq;
                 const int64_t row = (int64_t)bh * a.Nq + li;
 #pragma unroll
@@ -483,30 +512,30 @@ using namespace fm;
 
 // The kernel's shared-memory limit, set once per device: later launches (also
 // those captured into a graph) make no attribute call.
-template <int D, bool PRECISE>
+template <int D, bool PRECISE, bool FP8 = false>
 static bool fwd_smem_ready()
 {
-    constexpr int smem = FwdSmem<D>::kBytes;
+    constexpr int smem = FwdSmem<D, FP8>::kBytes;
     static_assert(smem <= 227 * 1024, "shared memory budget");
     static std::atomic<uint8_t> done[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load(std::memory_order_acquire)) return true;
-    if (cudaFuncSetAttribute(fm_fwd_kernel<D, PRECISE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(fm_fwd_kernel<D, PRECISE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return false;
     done[dev].store(1, std::memory_order_release);
     return true;
 }
 
-template <int D, bool PRECISE>
+template <int D, bool PRECISE, bool FP8 = false>
 static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const FwdArgs &a, cudaStream_t stream)
 {
-    constexpr int smem = FwdSmem<D>::kBytes;
-    if (!fwd_smem_ready<D, PRECISE>()) return FM_ERR_CUDA;
+    constexpr int smem = FwdSmem<D, FP8>::kBytes;
+    if (!fwd_smem_ready<D, PRECISE, FP8>()) return FM_ERR_CUDA;
     ProfScope ps(kKFwd, stream);
-    fm_fwd_kernel<D, PRECISE><<<dim3(a.L.n_q, a.H, a.B), 352, smem, stream>>>(tq, tk, tv, a);
+    fm_fwd_kernel<D, PRECISE, FP8><<<dim3(a.L.n_q, a.H, a.B), 352, smem, stream>>>(tq, tk, tv, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
@@ -515,6 +544,14 @@ fm_status fm_fwd_prepare(int d, bool precise)
     const bool ok = d == 128 ? (precise ? fwd_smem_ready<128, true>() : fwd_smem_ready<128, false>())
                              : (precise ? fwd_smem_ready<64, true>() : fwd_smem_ready<64, false>());
     return ok ? FM_OK : FM_ERR_CUDA;
+}
+
+fm_status fm_fwd_prepare_fp8() { return fwd_smem_ready<128, false, true>() ? FM_OK : FM_ERR_CUDA; }
+
+fm_status fm_fwd_launch_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
+                            const FwdArgs &a, cudaStream_t stream)
+{
+    return launch_fwd<128, false, true>(tq, tk, tvt, a, stream);
 }
 
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

@@ -145,6 +145,7 @@ struct FwdArgs {
     int q_row0, Nq;       // Q, O, lse hold rows [q_row0, q_row0 + Nq) of the mask
     float scale_log2;     // softmax scale * log2(e)
     int o_f32;
+    const float *descale; // FP8 path: device [3], the Q, K, V descales (else unused)
 };
 
 // Arguments of the backward main kernel.
@@ -172,6 +173,8 @@ enum KernelId {
     kKBwd = FM_K_BWD,
     kKBwdPost = FM_K_BWD_POST,
     kKClassifyOrder = FM_K_CLASSIFY_ORDER,
+    kKFp8Amax = FM_K_FP8_AMAX,
+    kKFp8Convert = FM_K_FP8_CONVERT,
 };
 
 // Devices a process may use (per-device caches of kernel attributes).

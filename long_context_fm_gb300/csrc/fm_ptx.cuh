@@ -407,4 +407,47 @@ __device__ __forceinline__ void red_add_f32(float *addr, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
+// ---- FP8 (e4m3) ---------------------------------------------------------------
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0 in
+// both fields), fp32 accumulate, both operands K-major: the kind::f16 layout
+// with other format codes.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N)
+{
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, e4m3 operands (one instruction: K = 32)
+__device__ __forceinline__ void mma_ss_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, e4m3 (A: 128 lanes x 32 bytes in 8 columns,
+// byte k of a lane's row = element k)
+__device__ __forceinline__ void mma_ts_e4m3(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two fp32 values to e4m3 (round to nearest even, saturating at +-448): `lo`
+// in bits 0-7, `hi` in bits 8-15.
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 }  // namespace fm

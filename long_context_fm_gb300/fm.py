@@ -24,13 +24,14 @@ FM_TILE_SKIP, FM_TILE_FULL, FM_TILE_PARTIAL = 0, 1, 2
 FM_DT_BF16, FM_DT_F32 = 0, 1
 FM_FLAG_PRECISE = 1
 KERNEL_NAMES = ["classify_minmax", "classify_lists", "fwd", "bwd_pre", "bwd", "bwd_post",
-                "classify_order"]
+                "classify_order", "fp8_amax", "fp8_convert"]
 
 EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_mask_from_row_intervals",
             "fm_plan_bytes", "fm_tile_classify", "fm_fwd_workspace_bytes", "fm_attn_fwd", "fm_bwd_workspace_bytes",
             "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
             "fm_attn_bwd_noalloc", "fm_step_graph_create", "fm_step_graph_launch", "fm_step_graph_destroy",
-            "fm_plan_bytes_rows", "fm_tile_classify_rows", "fm_attn_fwd_rows", "fm_attn_bwd_rows"]
+            "fm_plan_bytes_rows", "fm_tile_classify_rows", "fm_attn_fwd_rows", "fm_attn_bwd_rows",
+            "fm_quantize_fp8", "fm_attn_fwd_fp8"]
 # Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -92,6 +93,8 @@ _lib.fm_attn_fwd_rows.argtypes = [_P, _P, _P, Bounds, _P, _I, _I, _I, _I, _I, _I
                                   _P, _P]
 _lib.fm_attn_bwd_rows.argtypes = [_P, _P, _P, _P, _I, _P, _P, Bounds, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                   _P, _I, _I, _P, _SZ, _P, _P]
+_lib.fm_quantize_fp8.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _P]
+_lib.fm_attn_fwd_fp8.argtypes = [_P, _P, _P, _P, Bounds, _P, _I, _I, _I, _I, _F, _P, _I, _P, _P, _P]
 _lib.fm_step_graph_create.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(ctypes.c_void_p)]
 _lib.fm_step_graph_launch.argtypes = [_P, _P]
 _lib.fm_step_graph_destroy.argtypes = [_P]
@@ -334,6 +337,40 @@ def fm_attn_bwd_rows(q, k, v, o, lse, dO, bounds: Bounds, plan, q_row0, scale, d
                                  _ptr(dv), _dt(dq), int(flags), _ptr(ws), ws.numel(), _ptr(dev_status),
                                  _stream(stream))
     _check(code, "fm_attn_bwd_rows")
+
+
+def fm_quantize_fp8(x, transpose=False, out=None, descale=None, stream=None):
+    """Per-tensor e4m3 codes (uint8) of a bf16 [B, H, N, d] tensor and its
+    descale (device float32 [1]); transpose=True gives the [B, H, d, N] layout."""
+    _dev(x, torch.bfloat16, "x")
+    B, H, N, d = x.shape
+    shape = (B, H, d, N) if transpose else (B, H, N, d)
+    out = torch.empty(shape, dtype=torch.uint8, device=x.device) if out is None else _dev(out, torch.uint8, "out")
+    descale = torch.empty(1, dtype=torch.float32, device=x.device) if descale is None else descale
+    _dev(descale, torch.float32, "descale")
+    _check(_lib.fm_quantize_fp8(_ptr(x), B, H, N, d, int(bool(transpose)), _ptr(out), _ptr(descale),
+                                _stream(stream)), "fm_quantize_fp8")
+    return out, descale
+
+
+def fm_attn_fwd_fp8(q8, k8, vt8, descale, bounds: Bounds, plan, scale, o, lse, dev_status, stream=None):
+    """Forward on e4m3 q8, k8 [B, H, N, d] and vt8 [B, H, d, N]; descale: device
+    float32 [3] (Q, K, V)."""
+    for n, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        _dev(t, torch.uint8, n)
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or vt8.shape != (B, H, d, N) or o.shape != q8.shape:
+        raise ValueError("q8, k8, o: [B, H, N, d]; vt8: [B, H, d, N]")
+    _dev(descale, torch.float32, "descale")
+    if descale.numel() != 3:
+        raise ValueError("descale holds the Q, K and V descales")
+    _dev(o, o.dtype, "o")
+    _dev(lse, torch.float32, "lse")
+    _dev(plan, torch.uint8, "plan")
+    _dev(dev_status, torch.int32, "dev_status")
+    code = _lib.fm_attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(descale), bounds, _ptr(plan), B, H, N, d,
+                                float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(dev_status), _stream(stream))
+    _check(code, "fm_attn_fwd_fp8")
 
 
 def fm_step_graph_create(q, k, v, dO, bounds: Bounds, plan, scale, o, lse, dev_status, dq=None, dk=None,

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(fm):
 
 
 def test_abi_version_and_status_strings(fm):
-    assert fm.fm_abi_version() == 5
+    assert fm.fm_abi_version() == 6
     for code in range(9):
         assert fm.fm_status_string(code) and "unknown" not in fm.fm_status_string(code)
     assert "unknown" in fm.fm_status_string(99)
