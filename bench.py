@@ -41,9 +41,14 @@ from long_context_fm_gb300 import workloads as W  # noqa: E402
 METRIC = "fwd and fwd+bwd TFLOP/s on unmasked FLOPs (% of GB300 BF16 peak) at N=128K"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture, keyed by
-# the hash of the kernel source it was taken on (stale entries are ignored).
-NCU_TRAFFIC = {}
+# DRAM bytes (read + written) per launch of the dominant kernel from a 1-pass
+# ncu capture of dram__bytes_read.sum and dram__bytes_write.sum, keyed by the
+# kernel, the hash of the source it was taken on (stale entries are ignored)
+# and the workload.
+NCU_TRAFFIC = {
+    ("bwd", "87ae0d9e94820b43", "long_packing_128k"): 4.31e9 + 2.90e9,
+    ("bwd", "87ae0d9e94820b43", "sliding_window"): 831.54e6 + 762.06e6,
+}
 
 
 def load_peaks():
@@ -404,7 +409,7 @@ def main():
         peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         key = src_hash("fm_bwd.cu")
-        traffic = NCU_TRAFFIC.get(("bwd", key))
+        traffic = NCU_TRAFFIC.get(("bwd", key, wl.name))
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_step"],
