@@ -9,7 +9,8 @@ backward, 14d together); `value` is the fwd+bwd figure with inputs resident
 in HBM.  `e2e` repeats the step through the C ABI from pinned host buffers:
 row-form mask conversion on the host, host-to-device copies of Q, K, V, dO
 and the bounds, the device work, and device-to-host copies of O, lse, dQ,
-dK, dV, all inside the timed region.  `graph` times the same step captured
+dK, dV, all inside the timed region; the copies run on their own streams
+with two buffer sets, so one step's copies overlap its neighbours' compute.  `graph` times the same step captured
 once into a CUDA graph (fm_step_graph_create) and replayed, one launch per
 step.  `fp8_fwd` times the forward on e4m3 inputs (fm_attn_fwd_fp8) and the
 quantization of Q, K, V beside it.
@@ -262,43 +263,86 @@ def run_fm(args, rank, world, local_rank):
             raise RuntimeError(f"device status {int(status.item())} in the FP8 forward")
         fp8 = (f0.elapsed_time(f1) / args.steps, f1.elapsed_time(f2) / args.steps)
 
-    # ---- end to end through the C ABI from pinned host buffers
+    # ---- end to end through the C ABI from pinned host buffers, pipelined:
+    # host-to-device copies, the step and device-to-host copies run on three
+    # streams with two buffer sets, so the copies of one step overlap the
+    # compute of its neighbours; every step still copies its own inputs in and
+    # its own outputs out inside the timed region.
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, dO))
     rows = m["rows"]
-    ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
-    hdq, hdk, hdv = (torch.empty_like(dq, device="cpu").pin_memory() for _ in range(3))
-    hb = [torch.empty(bnd[0].shape, dtype=torch.int32).pin_memory() for _ in range(4)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * hb[0].numel() * 4
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hl, hdq, hdk, hdv))
-
     multi = m["row_intervals"]
 
-    def e2e_step():
+    def device_set(first):
+        if first:
+            return dict(q=q, k=k, v=v, dO=dO, o=o, lse=lse, dq=dq, dk=dk, dv=dv, bnd=bnd, bounds=bounds)
+        st = dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v), dO=torch.empty_like(dO),
+                  o=torch.empty_like(o), lse=torch.empty_like(lse), dq=torch.empty_like(dq),
+                  dk=torch.empty_like(dk), dv=torch.empty_like(dv), bnd=[torch.empty_like(b) for b in bnd])
+        st["bounds"] = fm.make_bounds(*st["bnd"])
+        return st
+
+    sets = [device_set(True), device_set(False)]
+    host_out = [dict((key, torch.empty_like(sets[0][key], device="cpu").pin_memory())
+                     for key in ("o", "lse", "dq", "dk", "dv")) for _ in range(2)]
+    host_bnd = [[torch.empty(bnd[0].shape, dtype=torch.int32).pin_memory() for _ in range(4)] for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * bnd[0].numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+    s_h2d, s_cmp, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_h2d = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_issue(i):
+        sidx = i % 2
+        bs, hb = sets[sidx], host_bnd[sidx]
         if rows is not None:                                     # host conversion of the row form
             cols = fm.fm_mask_from_rows(*rows)
         elif multi is not None:                                  # several intervals per row
             cols = fm.fm_mask_from_row_intervals(*multi)
         else:
             cols = [m[x] for x in ("lts", "lte", "uts", "ute")]
+        if i >= 2:
+            ev_h2d[sidx].synchronize()                           # hb is still being copied from
         for dst, src in zip(hb, cols):
             dst.numpy()[...] = src
-        for dst, src in zip(bnd, hb):
-            dst.copy_(src, non_blocking=True)
-        for dst, src in zip((q, k, v, dO), (hq, hk, hv, hdo)):
-            dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in zip((ho, hl, hdq, hdk, hdv), (o, lse, dq, dk, dv)):
-            dst.copy_(src, non_blocking=True)
-        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(ev_cmp[sidx])                   # the set's inputs are free again
+            for dst, src in zip(bs["bnd"], hb):
+                dst.copy_(src, non_blocking=True)
+            for key, src in zip(("q", "k", "v", "dO"), (hq, hk, hv, hdo)):
+                bs[key].copy_(src, non_blocking=True)
+            ev_h2d[sidx].record(s_h2d)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_h2d[sidx])
+            if i >= 2:
+                s_cmp.wait_event(ev_d2h[sidx])                   # the set's outputs have been read out
+            fm.fm_tile_classify(bs["bounds"], plan, status, stream=s_cmp)
+            fm.fm_attn_fwd(bs["q"], bs["k"], bs["v"], bs["bounds"], plan, scale, bs["o"], bs["lse"], status,
+                           stream=s_cmp)
+            fm.fm_attn_bwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["lse"], bs["dO"], bs["bounds"], plan, scale,
+                           bs["dq"], bs["dk"], bs["dv"], ws, status, stream=s_cmp)
+            ev_cmp[sidx].record(s_cmp)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_cmp[sidx])
+            for key, dst in host_out[sidx].items():
+                dst.copy_(bs[key], non_blocking=True)
+            ev_d2h[sidx].record(s_d2h)
 
-    e2e_step()
+    torch.cuda.synchronize(dev)
+    for i in range(2):
+        e2e_issue(i)
+    torch.cuda.synchronize(dev)
     barrier()
+    e2e_steps = max(2, min(args.steps, 8))
     t0 = time.perf_counter()
-    e2e_steps = max(1, min(args.steps, 5))
-    for _ in range(e2e_steps):
-        e2e_step()
+    for i in range(e2e_steps):
+        e2e_issue(i + 2)
+    torch.cuda.synchronize(dev)
     barrier()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the end-to-end steps")
 
     ms_step, e2e_s, graph_ms = max_over_ranks([ms_step, e2e_s, graph_ms], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
