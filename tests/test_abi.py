@@ -297,3 +297,15 @@ def test_step_graph_null_arguments(fm):
     assert fm._lib.fm_step_graph_launch(None, None) == fm.FM_ERR_INVALID_ARG
     assert fm._lib.fm_step_graph_destroy(None) == fm.FM_ERR_INVALID_ARG
     assert ctypes.sizeof(fm.StepArgs) == 200                 # the C layout on LP64
+
+
+def test_binding_fails_loudly_without_the_library():
+    """No CPU fallback: importing the binding without libfm.so raises, naming the build step."""
+    import subprocess
+    import sys
+    code = ("import os; real = os.path.exists; "
+            "os.path.exists = lambda p: False if str(p).endswith('libfm.so') else real(p); "
+            "import long_context_fm_gb300.fm")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "build" in r.stderr
