@@ -10,12 +10,17 @@
 // One CTA = one (b, h, 128-row Q tile); it walks the plan's list of non-skip
 // KV tiles (staged in shared memory); skip tiles are never loaded.  Roles:
 //   warp 0      TMA producer of Q (once) and K (three-stage ring)
-//   warp 1      allocates TMEM; one thread issues the tcgen05 MMAs
+//   warp 1      allocates TMEM; one thread issues the Q K^T MMAs
 //   warps 2-5   softmax, KV columns [0, 64) of every row (thread = row =
 //               TMEM lane)
 //   warps 6-9   softmax, KV columns [64, 128)
 //   warp 10     TMA producer of V (two-stage ring); stages the column bounds
 //               of partial tiles with it
+//   warp 11     one thread issues the P V MMAs
+// Two issuing threads: the scores of later tiles are issued as soon as
+// their K and score buffer are free, independently of the P V products
+// waiting for the softmax (one thread doing both spent ~3,000 cycles per tile
+// in waits and issue; the two streams now overlap).
 // TMEM (512 columns): three score buffers S_0, S_1, S_2 at [0, 128),
 // [128, 256), [256, 384) (tile t uses S_{t mod 3}) and O at [384, 384 + d).
 // The scores of tile t + 1 are computed while the softmax works on tile t;
@@ -76,7 +81,7 @@ constexpr int kSB = 3;              // score buffers in TMEM
 constexpr int kSoftmaxBar = 1;      // named barrier of the two softmax warpgroups (256 threads)
 
 template <int D, bool PRECISE, bool FP8>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(384, 1)
     fm_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a)
 {
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(352, 1)
                 mbar_init(&bars[FB_P0 + s], 256);
                 mbar_init(&bars[FB_O0 + s], 1);
             }
-            mbar_init(&bars[FB_DRAIN], 1);
+            mbar_init(&bars[FB_DRAIN], 2);      // both MMA issuers commit
             fence_barrier_init();
         }
     }
@@ -252,21 +257,19 @@ __global__ void __launch_bounds__(352, 1)
                 for (int k2 = (nv > VS ? nv - VS : 0); k2 < nv; ++k2)
                     mbar_wait_drain(&bars[FB_VF0 + (k2 % VS)], (k2 / VS) & 1, a.status);
         } else if (warp == 1) {
-            // ------------------------------------------------ MMA issuer
-            // S of tile t + 2 is issued before the PV of tile t (which waits for the
-            // softmax of tile t), as soon as its K has landed and its score buffer
-            // has been read by the PV of tile t - 1.
+            // ------------------------------------------------ S issuer
+            // The scores of tile t as soon as its K has landed and its score buffer
+            // has been read by the PV of tile t - 3; runs ahead of the softmax by up
+            // to the three score buffers.
             if (lane == 0 && n > 0) {
                 constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-                constexpr uint32_t idO = idesc_bf16(128, D, false, true);
-                constexpr int NPART = PRECISE ? 2 : 1;
                 const uint64_t dQ = sdesc_sw128(smem_u32(smem + S::kQ), 16, 1024);
-                const uint32_t tO = tmem + 384;
-                auto issue_S = [&](int t) -> bool {
+                bool ok = mbar_wait(&bars[FB_Q], 0, abort, a.status);
+                for (int t = 0; ok && t < n; ++t) {
                     const int ks = t % KS;
-                    if (!mbar_wait(&bars[FB_KF0 + ks], (t / KS) & 1, abort, a.status)) return false;
+                    if (!mbar_wait(&bars[FB_KF0 + ks], (t / KS) & 1, abort, a.status)) break;
                     // The buffer's previous tile, t - 3, must have finished its PV.
-                    if (t >= kSB && !mbar_wait(&bars[FB_O0 + t % kSB], ((t - kSB) / kSB) & 1, abort, a.status)) return false;
+                    if (t >= kSB && !mbar_wait(&bars[FB_O0 + t % kSB], ((t - kSB) / kSB) & 1, abort, a.status)) break;
                     tc_fence_after();
                     const uint64_t dK = sdesc_sw128(smem_u32(smem + S::kK + ks * S::kTile), 16, 1024);
                     const uint32_t tS = tmem + (t % kSB) * 128;
@@ -283,17 +286,25 @@ __global__ void __launch_bounds__(352, 1)
                     }
                     tc_commit(&bars[FB_S0 + t % kSB]);
                     tc_commit(&bars[FB_KE0 + ks]);
-                    return true;
-                };
-                bool ok = mbar_wait(&bars[FB_Q], 0, abort, a.status) && issue_S(0) && (n < 2 || issue_S(1));
-                for (int t = 0; ok && t < n; ++t) {
-                    if (t + 2 < n && !(ok = issue_S(t + 2))) break;
+                }
+            }
+            if (lane == 0) {
+                // Every MMA of this CTA (both issuers) completes before TMEM is released.
+                tc_commit(&bars[FB_DRAIN]);
+                mbar_wait_drain(&bars[FB_DRAIN], 0, a.status);
+            }
+        } else if (warp == 11) {
+            // ------------------------------------------------ PV issuer
+            // O += P V of tile t once the softmax has written P and V has landed.
+            if (lane == 0 && n > 0) {
+                constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+                constexpr int NPART = PRECISE ? 2 : 1;
+                const uint32_t tO = tmem + 384;
+                for (int t = 0; t < n; ++t) {
                     const int vs = t % VS;
                     if (!mbar_wait(&bars[FB_VF0 + vs], (t / VS) & 1, abort, a.status) ||
-                        !mbar_wait(&bars[FB_P0 + t % kSB], (t / kSB) & 1, abort, a.status)) {
-                        ok = false;
+                        !mbar_wait(&bars[FB_P0 + t % kSB], (t / kSB) & 1, abort, a.status))
                         break;
-                    }
                     tc_fence_after();
                     const uint32_t tP = tmem + (t % kSB) * 128;
                     if (FP8) {
@@ -316,7 +327,6 @@ __global__ void __launch_bounds__(352, 1)
                 }
             }
             if (lane == 0) {
-                // Every MMA of this CTA completes before TMEM is released.
                 tc_commit(&bars[FB_DRAIN]);
                 mbar_wait_drain(&bars[FB_DRAIN], 0, a.status);
             }
@@ -535,7 +545,7 @@ static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
     constexpr int smem = FwdSmem<D, FP8>::kBytes;
     if (!fwd_smem_ready<D, PRECISE, FP8>()) return FM_ERR_CUDA;
     ProfScope ps(kKFwd, stream);
-    fm_fwd_kernel<D, PRECISE, FP8><<<dim3(a.L.n_q, a.H, a.B), 352, smem, stream>>>(tq, tk, tv, a);
+    fm_fwd_kernel<D, PRECISE, FP8><<<dim3(a.L.n_q, a.H, a.B), 384, smem, stream>>>(tq, tk, tv, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
