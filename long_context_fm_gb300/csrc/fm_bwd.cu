@@ -13,12 +13,16 @@
 //   warp 0      TMA producer (K and V once; Q, dO halves in a ring of three
 //               stages, two in precise mode; lse and D staged into shared
 //               memory by the whole warp)
-//   warp 1      TMEM allocation; one thread issues the score MMAs (S^T, dP^T)
+//   warp 1      TMEM allocation; one thread issues the S^T MMAs
 //   warps 2-17  four warpgroups, one thread per KV row j each: P^T and dS^T
 //               for 16 of the half's 64 columns each
 //   warps 18-21 one thread per head-dim index: drain dQ^T from TMEM into the
 //               fp32 dQ accumulator with red.global.add
-//   warp 22     one thread issues the gradient MMAs (dV, dK, dQ^T)
+//   warp 22     one thread issues the dQ^T MMAs
+//   warp 23     one thread issues the dP^T MMAs
+//   warp 24     one thread issues the dV, then dK MMAs
+// The four issuing threads sit on four different sub-partitions, each
+// product stream waiting only for its own inputs.
 // TMEM (512 columns): dK [0, d), dV [128, 128 + d), two score buffers
 // b = half & 1 with S^T [256 + 128 b, +64) and dP^T [320 + 128 b, +64); the
 // half's dQ^T lands in the S^T columns after P^T/dS^T are written, so the
@@ -152,7 +156,7 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
 
 
 template <int D, bool PRECISE>
-__global__ void __launch_bounds__(736, 1)
+__global__ void __launch_bounds__(800, 1)
     fm_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdArgs a)
@@ -207,23 +211,23 @@ __global__ void __launch_bounds__(736, 1)
             mbar_init(&bars[BB_KV], 1);
             for (int s2 = 0; s2 < NST; ++s2) {
                 mbar_init(&bars[BB_QF0 + s2], 33);
-                mbar_init(&bars[BB_QE0 + s2], 2);     // scores and gradients issuers
+                mbar_init(&bars[BB_QE0 + s2], 3);     // S^T, dP^T and dV/dK issuers
             }
-            mbar_init(&bars[BB_SF0], 1);
-            mbar_init(&bars[BB_SF1], 1);
+            mbar_init(&bars[BB_SF0], 2);      // S^T and dP^T issuers
+            mbar_init(&bars[BB_SF1], 2);
             mbar_init(&bars[BB_DF0], 512);    // four P/dS warpgroups: dS^T written
             mbar_init(&bars[BB_DF1], 512);
             mbar_init(&bars[BB_PF0], 512);    // P^T written
             mbar_init(&bars[BB_PF1], 512);
             mbar_init(&bars[BB_PE], 1);
-            mbar_init(&bars[BB_DSE0], 1);
-            mbar_init(&bars[BB_DSE1], 1);
+            mbar_init(&bars[BB_DSE0], 2);     // dQ^T and dK read dS^T
+            mbar_init(&bars[BB_DSE1], 2);
             mbar_init(&bars[BB_DQF0], 1);
             mbar_init(&bars[BB_DQF1], 1);
             mbar_init(&bars[BB_DQE0], 128);
             mbar_init(&bars[BB_DQE1], 128);
             mbar_init(&bars[BB_ACC], 1);
-            mbar_init(&bars[BB_DRAIN0], 1);
+            mbar_init(&bars[BB_DRAIN0], 4);   // all four issuers
             mbar_init(&bars[BB_DRAIN1], 1);
             fence_barrier_init();
         }
@@ -311,16 +315,15 @@ __global__ void __launch_bounds__(736, 1)
                 for (int k2 = (it > NST ? it - NST : 0); k2 < it; ++k2)
                     mbar_wait_drain(&bars[BB_QF0 + (k2 % NST)], (k2 / NST) & 1, a.status);
             }
-        } else if (warp == 1 || warp == 22) {
+        } else if (warp == 1 || warp >= 22) {
             // ------------------------------------------------ MMA issuers
-            // Two issuing threads: warp 1 issues the scores S^T, dP^T of each
-            // half as soon as its Q/dO have landed and the S buffer is drained;
-            // warp 22 issues the gradient products dV, dK, dQ^T of each half as
-            // soon as its P/dS are written.  Each blocks on the tensor-core
-            // queue independently, so the next scores are never held back
-            // behind the current gradients (or the reverse).  A Q/dO stage is
-            // released by one commit from each thread.
-            const bool scores = (warp == 1);
+            // Four issuing threads, one per product stream, each in a warp of its
+            // own sub-partition: warp 1 S^T and warp 23 dP^T of each half (as soon
+            // as its Q/dO have landed and the score buffer is drained), warp 22
+            // dQ^T (once dS^T is written), warp 24 dV then dK (once P^T, dS^T are
+            // written).  A Q/dO stage is released by the S^T, dP^T and dV/dK
+            // threads, a dS^T buffer by the dQ^T and dK products.
+            const int role = (warp == 1) ? 0 : (warp == 23) ? 1 : (warp == 22) ? 2 : 3;
             if (lane == 0 && n_it > 0) {
                 constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
                 constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
@@ -336,80 +339,71 @@ __global__ void __launch_bounds__(736, 1)
                 bool ok = mbar_wait(&bars[BB_KV], 0, abort, a.status);
                 for (int it = 0; ok && it < n_it; ++it) {
                     const int st = it % NST;
-                    const uint64_t dQk = sdesc_sw128(smem_u32(sQ + st * S::kQTile), 16, 1024);
-                    const uint64_t dOk = sdesc_sw128(smem_u32(sdO + st * S::kQTile), 16, 1024);
-                    if (scores) {
+                    if (role <= 1) {
                         const int b = it & 1;
                         // Buffer b is free once the drain holds the dQ^T of the half
                         // that used it before (which also implies its S^T, dP^T were read).
                         if (!mbar_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status) ||
                             (it >= 2 && !mbar_wait(&bars[BB_DQE0 + b], ((it >> 1) - 1) & 1, abort, a.status))) { ok = false; break; }
                         tc_fence_after();
+                        const uint64_t dA = role == 0 ? dKk : dVk;                    // K for S^T, V for dP^T
+                        const uint64_t dB = sdesc_sw128(smem_u32((role == 0 ? sQ : sdO) + st * S::kQTile), 16, 1024);
+                        const uint32_t tD = (role == 0 ? tS0 : tdP0) + b * 128;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
                             const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tS0 + b * 128, sdesc_add(dKk, ok_), sdesc_add(dQk, oq), idS, kk > 0);
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
-                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tdP0 + b * 128, sdesc_add(dVk, ok_), sdesc_add(dOk, oq), idS, kk > 0);
+                            mma_ss(tD, sdesc_add(dA, ok_), sdesc_add(dB, oq), idS, kk > 0);
                         }
                         tc_commit(&bars[BB_SF0 + b]);
                         tc_commit(&bars[BB_QE0 + st]);
                     } else {
                         const int qb = it & 1;         // score buffer: dQ^T goes into its S^T columns
-                        if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
-                        const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
                         const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;   // dS^T buffer of this half
                         const uint32_t pbo = pb * S::kOp;
-                        // dQ^T first: the score buffer it lands in is the one the
-                        // scores of half it + 2 wait for; dV next: the single P^T
-                        // tile it frees is the next thing the P/dS warps wait for.
-                        // Each commit releases its inputs as early as possible: the
-                        // score buffer (through the drain) after dQ^T, P^T after dV,
-                        // dS^T and the Q/dO stage after dK.
+                        if (role == 2) {
+                            if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                            tc_fence_after();
 #pragma unroll
-                        for (int part = 0; part < NPART; ++part)
+                            for (int part = 0; part < NPART; ++part)
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                mma_ss(tS0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048), idQ,
-                                       (part > 0 || kk > 0));
-                        tc_commit(&bars[BB_DQF0 + qb]);
-                        if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status)) {
-                            ok = false;
-                            break;
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_ss(tS0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048),
+                                           idQ, (part > 0 || kk > 0));
+                            tc_commit(&bars[BB_DQF0 + qb]);
+                            tc_commit(&bars[BB_DSE0 + pb]);
+                        } else {
+                            const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
+                            const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
+                            if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                            tc_fence_after();
+#pragma unroll
+                            for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                           (it > 0 || part > 0 || kk > 0));
+                            tc_commit(&bars[BB_PE]);
+                            // dS^T was written before P^T (the P/dS warps' order), so
+                            // P^T written implies dS^T written: this wait is immediate.
+                            if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                            tc_fence_after();
+#pragma unroll
+                            for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
+                                           (it > 0 || part > 0 || kk > 0));
+                            tc_commit(&bars[BB_DSE0 + pb]);
+                            tc_commit(&bars[BB_QE0 + st]);
                         }
-                        tc_fence_after();
-#pragma unroll
-                        for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
-                                       (it > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[BB_PE]);
-#pragma unroll
-                        for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
-                                       (it > 0 || part > 0 || kk > 0));
-                        tc_commit(&bars[BB_DSE0 + pb]);
-                        tc_commit(&bars[BB_QE0 + st]);
                     }
                 }
-                if (ok && !scores) tc_commit(&bars[BB_ACC]);
+                if (ok && role == 3) tc_commit(&bars[BB_ACC]);
             }
             if (lane == 0) {
-                tc_commit(&bars[BB_DRAIN0 + (scores ? 0 : 1)]);
-                mbar_wait_drain(&bars[BB_DRAIN0 + (scores ? 0 : 1)], 0, a.status);
+                tc_commit(&bars[BB_DRAIN0]);
+                mbar_wait_drain(&bars[BB_DRAIN0], 0, a.status);
             }
         } else if (warp < 18) {
             // ------------------------------------------------ P^T / dS^T
@@ -648,7 +642,7 @@ static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
     constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
     if (!bwd_smem_ready<D, PRECISE>()) return FM_ERR_CUDA;
     ProfScope ps(kKBwd, stream);
-    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 736, smem, stream>>>(tq, tk, tv, tdo, a);
+    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 800, smem, stream>>>(tq, tk, tv, tdo, a);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
