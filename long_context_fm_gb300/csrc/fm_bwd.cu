@@ -24,18 +24,20 @@
 // The four issuing threads sit on four different sub-partitions, each
 // product stream waiting only for its own inputs.
 // TMEM (512 columns): dK [0, d), dV [128, 128 + d), two score buffers
-// b = half & 1 with S^T [256 + 128 b, +64) and dP^T [320 + 128 b, +64); the
-// half's dQ^T lands in the S^T columns after P^T/dS^T are written, so the
-// scores of the next half run while this half is still being processed.
+// b = half & 1 with S^T [256 + 128 b, +64) and dP^T [320 + 128 b, +64).  Each
+// thread overwrites the S^T columns it has read with its P^T as packed bf16
+// (the A operand of dV), and the half's dQ^T lands in the dP^T columns after
+// dS^T is written, so the scores of the next half run while this half is
+// still being processed.
 // Per half (M = 128 KV rows):
 //   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
 //   dP^T = V dO^T       (SS, K-major/K-major)        -> TMEM
 //   P^T  = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T o (dP^T - D)
-//          written as bf16 into 128-byte-swizzled shared memory (precise
-//          mode: as two bf16 terms hi + lo, ~16 significant bits, both
-//          consumed by the MMAs below, so the gradients do not carry a bf16
-//          rounding of P or dS)
-//   dV  += P^T dO       (SS, P^T K-major, dO MN-major)
+//          P^T written as bf16 into TMEM, dS^T into 128-byte-swizzled
+//          shared memory (precise mode: each as two bf16 terms hi + lo, ~16
+//          significant bits, both consumed by the MMAs below, so the
+//          gradients do not carry a bf16 rounding of P or dS)
+//   dV  += P^T dO       (TS, P^T from TMEM, dO MN-major)
 //   dK  += dS^T Q       (SS, dS^T K-major, Q MN-major)
 //   dQ^T = K^T dS^T     (SS, K MN-major, dS^T MN-major)
 #include <cuda.h>
@@ -111,12 +113,11 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, v
 // ---------------------------------------------------------------- main kernel
 template <int D, bool PRECISE>
 struct BwdSmem {
-    // Standard mode: three Q/dO stages (a stage's next load is in flight
-    // while the two halves before it are processed), one P^T tile (free as
-    // soon as dV has read it) and two dS^T tiles (dK and dQ^T of half i still
-    // read dS^T while half i+1 is written).  Precise mode keeps two stages and
-    // single operand tiles: the low operand terms take that room.
-    static constexpr int kStages = PRECISE ? 2 : 3;
+    // Three Q/dO stages (a stage's next load is in flight while the two
+    // halves before it are processed).  Standard mode keeps two dS^T tiles
+    // (dK and dQ^T of half i still read dS^T while half i+1 is written);
+    // precise mode one, the low terms taking the room of the second.
+    static constexpr int kStages = 3;
     static constexpr int kdSBufs = PRECISE ? 1 : 2;
     static constexpr int kKBox = 128 * 128;     // 64 columns x 128 rows
     static constexpr int kQBox = 64 * 128;      // 64 columns x 64 rows
@@ -126,15 +127,13 @@ struct BwdSmem {
     static constexpr int kK = 0, kV = kKTile;
     static constexpr int kQ = 2 * kKTile;                   // [kStages]
     static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
-    static constexpr int kP = kdO + kStages * kQTile;       // P^T  (high part)
-    static constexpr int kdS = kP + kOp;                    // dS^T (high part)  [kdSBufs]
-    static constexpr int kPlo = kdS + kdSBufs * kOp;        // precise: P^T low part
-    static constexpr int kdSlo = kPlo + kOp;                // precise: dS^T low part
-    static constexpr int kList = PRECISE ? kdSlo + kOp : kPlo;
+    static constexpr int kdS = kdO + kStages * kQTile;      // dS^T (high part)  [kdSBufs]
+    static constexpr int kdSlo = kdS + kdSBufs * kOp;       // precise: dS^T low part
+    static constexpr int kList = PRECISE ? kdSlo + kOp : kdSlo;
     static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
     static constexpr int kStat = kList + kListCap * 4;      // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
-    static constexpr int kNumBar = 23;
+    static constexpr int kNumBar = 24;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
@@ -142,7 +141,7 @@ struct BwdSmem {
 
 enum {
     BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_DF0, BB_DF1, BB_PF0, BB_PF1,
-    BB_PE, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1
+    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1
 };
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
@@ -171,7 +170,7 @@ __global__ void __launch_bounds__(800, 1)
     uint8_t *smem = smem_raw;
     uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
     uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
-    uint8_t *sP = smem + S::kP, *sdS = smem + S::kdS, *sPlo = smem + S::kPlo, *sdSlo = smem + S::kdSlo;
+    uint8_t *sdS = smem + S::kdS, *sdSlo = smem + S::kdSlo;
     int32_t *sList = reinterpret_cast<int32_t *>(smem + S::kList);
     constexpr int NST = S::kStages;
     float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [NST][64]
@@ -219,7 +218,8 @@ __global__ void __launch_bounds__(800, 1)
             mbar_init(&bars[BB_DF1], 512);
             mbar_init(&bars[BB_PF0], 512);    // P^T written
             mbar_init(&bars[BB_PF1], 512);
-            mbar_init(&bars[BB_PE], 1);
+            mbar_init(&bars[BB_PE0], 1);      // dV has read P^T
+            mbar_init(&bars[BB_PE1], 1);
             mbar_init(&bars[BB_DSE0], 2);     // dQ^T and dK read dS^T
             mbar_init(&bars[BB_DSE1], 2);
             mbar_init(&bars[BB_DQF0], 1);
@@ -244,9 +244,8 @@ __global__ void __launch_bounds__(800, 1)
     const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
     const int bh = b * a.H + h;
     const int kb = kt * 128;
-    // TMEM: dK, dV, S^T, dP^T, and dQ^T double-buffered (half it uses buffer it & 1).
-    // Score buffer b = half & 1: S^T at 256 + 128 b, dP^T at 320 + 128 b; the
-    // half's dQ^T reuses the S^T columns once P^T/dS^T have been written.
+    // TMEM: dK, dV, then two score buffers b = half & 1: S^T at 256 + 128 b
+    // (then P^T), dP^T at 320 + 128 b (then dQ^T, once dS^T has been written).
     const uint32_t tdK = tmem, tdV = tmem + 128, tS0 = tmem + 256, tdP0 = tmem + 320;
     const int cnt = *cnt_sh;
     const int32_t *glist =
@@ -319,7 +318,7 @@ __global__ void __launch_bounds__(800, 1)
             // ------------------------------------------------ MMA issuers
             // Four issuing threads, one per product stream, each in a warp of its
             // own sub-partition: warp 1 S^T and warp 23 dP^T of each half (as soon
-            // as its Q/dO have landed and the score buffer is drained), warp 22
+            // as its Q/dO have landed and their columns are free again), warp 22
             // dQ^T (once dS^T is written), warp 24 dV then dK (once P^T, dS^T are
             // written).  A Q/dO stage is released by the S^T, dP^T and dV/dK
             // threads, a dS^T buffer by the dQ^T and dK products.
@@ -332,7 +331,6 @@ __global__ void __launch_bounds__(800, 1)
                 const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024);      // K, K-major
                 const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);      // V, K-major
                 const uint64_t dKm = sdesc_sw128(smem_u32(sK), S::kKBox, 1024); // K, MN-major
-                const uint64_t dP[2] = {sdesc_sw128(smem_u32(sP), 16, 1024), sdesc_sw128(smem_u32(sPlo), 16, 1024)};
                 const uint64_t dSk[2] = {sdesc_sw128(smem_u32(sdS), 16, 1024), sdesc_sw128(smem_u32(sdSlo), 16, 1024)};
                 const uint64_t dSm[2] = {sdesc_sw128(smem_u32(sdS), S::kKBox, 1024),
                                          sdesc_sw128(smem_u32(sdSlo), S::kKBox, 1024)};
@@ -341,10 +339,12 @@ __global__ void __launch_bounds__(800, 1)
                     const int st = it % NST;
                     if (role <= 1) {
                         const int b = it & 1;
-                        // Buffer b is free once the drain holds the dQ^T of the half
-                        // that used it before (which also implies its S^T, dP^T were read).
+                        // The S^T columns of buffer b are free once dV has read the P^T
+                        // of the half that used them before, the dP^T columns once the
+                        // drain holds that half's dQ^T (both imply the scores were read).
+                        uint64_t *free_bar = &bars[(role == 0 ? BB_PE0 : BB_DQE0) + b];
                         if (!mbar_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status) ||
-                            (it >= 2 && !mbar_wait(&bars[BB_DQE0 + b], ((it >> 1) - 1) & 1, abort, a.status))) { ok = false; break; }
+                            (it >= 2 && !mbar_wait(free_bar, ((it >> 1) - 1) & 1, abort, a.status))) { ok = false; break; }
                         tc_fence_after();
                         const uint64_t dA = role == 0 ? dKk : dVk;                    // K for S^T, V for dP^T
                         const uint64_t dB = sdesc_sw128(smem_u32((role == 0 ? sQ : sdO) + st * S::kQTile), 16, 1024);
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(800, 1)
                         tc_commit(&bars[BB_SF0 + b]);
                         tc_commit(&bars[BB_QE0 + st]);
                     } else {
-                        const int qb = it & 1;         // score buffer: dQ^T goes into its S^T columns
+                        const int qb = it & 1;         // score buffer: P^T in its S^T columns, dQ^T in its dP^T columns
                         const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;   // dS^T buffer of this half
                         const uint32_t pbo = pb * S::kOp;
                         if (role == 2) {
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(800, 1)
                             for (int part = 0; part < NPART; ++part)
 #pragma unroll
                                 for (int kk = 0; kk < 8; ++kk)
-                                    mma_ss(tS0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048),
+                                    mma_ss(tdP0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048),
                                            idQ, (part > 0 || kk > 0));
                             tc_commit(&bars[BB_DQF0 + qb]);
                             tc_commit(&bars[BB_DSE0 + pb]);
@@ -377,15 +377,15 @@ __global__ void __launch_bounds__(800, 1)
                             const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
                             if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
                             tc_fence_after();
+                            // P^T of the 16 columns kk: TMEM columns [16 kk, 16 kk + 8) of
+                            // the S^T block (the low terms in the next 8 columns).
 #pragma unroll
                             for (int part = 0; part < NPART; ++part)
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
-                                    mma_ss(tdV, sdesc_add(dP[part], kk * 32), sdesc_add(dOm, kk * 2048), idKV,
+                                    mma_ts(tdV, tS0 + qb * 128 + kk * 16 + part * 8, sdesc_add(dOm, kk * 2048), idKV,
                                            (it > 0 || part > 0 || kk > 0));
-                            tc_commit(&bars[BB_PE]);
-                            // dS^T was written before P^T (the P/dS warps' order), so
-                            // P^T written implies dS^T written: this wait is immediate.
+                            tc_commit(&bars[BB_PE0 + qb]);
                             if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
                             tc_fence_after();
 #pragma unroll
@@ -467,13 +467,30 @@ __global__ void __launch_bounds__(800, 1)
                     }
                     p[c] = p0;
                     p[c + 1] = p1;
-                    const uint64_t t2 = f2_sub(f2_pack(__uint_as_float(draw[c]), __uint_as_float(draw[c + 1])), dd2[c / 2]);
-                    f2_unpack(f2_mul(f2_pack(p0, p1), t2), ds[c], ds[c + 1]);
                 }
-                // dS^T first (its buffer is free once dK, dQ^T of the half that
-                // last used it have completed, normally long ago), announced on
-                // DF so that dQ^T can start; then P^T, whose single tile is free
-                // once dV of the previous half has read it, announced on PF.
+                // P^T into the S^T columns this thread has read: bf16 pairs in
+                // columns [c0, c0 + 8) (precise: low terms in [c0 + 8, c0 + 16)).
+                if (PRECISE) {
+                    uint32_t pw[16];
+#pragma unroll
+                    for (int w2 = 0; w2 < 8; ++w2) split_bf16x2(p[2 * w2], p[2 * w2 + 1], pw[w2], pw[8 + w2]);
+                    tmem_st16(tS0 + b * 128 + lane_off + c0, pw);
+                } else {
+                    uint32_t pw[8];
+#pragma unroll
+                    for (int w2 = 0; w2 < 8; ++w2) pw[w2] = pack_bf16x2(p[2 * w2], p[2 * w2 + 1]);
+                    tmem_st8(tS0 + b * 128 + lane_off + c0, pw);
+                }
+#pragma unroll
+                for (int c = 0; c < CW; c += 2) {
+                    const uint64_t t2 = f2_sub(f2_pack(__uint_as_float(draw[c]), __uint_as_float(draw[c + 1])), dd2[c / 2]);
+                    f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t2), ds[c], ds[c + 1]);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars[BB_PF0 + b]);
+                // dS^T (its buffer is free once dK, dQ^T of the half that last
+                // used it have completed, normally long ago), announced on DF.
                 const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;
                 const int back = S::kdSBufs;                 // halves between two uses of a dS^T buffer
                 if (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status)) { ok = false; break; }
@@ -494,25 +511,8 @@ __global__ void __launch_bounds__(800, 1)
                     if (PRECISE) *reinterpret_cast<uint4 *>(sdSlo + off) = make_uint4(dl[0], dl[1], dl[2], dl[3]);
                 }
                 fence_proxy_async_smem();
-                tc_fence_before();                  // S^T, dP^T reads of this half precede the dQ^T MMA
+                tc_fence_before();                  // dP^T reads of this half precede the dQ^T MMA
                 mbar_arrive(&bars[BB_DF0 + b]);
-                if (it >= 1 && !warp_wait(&bars[BB_PE], (it - 1) & 1, abort, a.status)) { ok = false; break; }
-#pragma unroll
-                for (int u = 0; u < CW / 8; ++u) {
-                    const int chunk = (c0 >> 3) + u;
-                    const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
-                    uint32_t ph[4], pl[4];
-#pragma unroll
-                    for (int w2 = 0; w2 < 4; ++w2) {
-                        const int c = 8 * u + 2 * w2;
-                        if (PRECISE) split_bf16x2(p[c], p[c + 1], ph[w2], pl[w2]);
-                        else ph[w2] = pack_bf16x2(p[c], p[c + 1]);
-                    }
-                    *reinterpret_cast<uint4 *>(sP + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-                    if (PRECISE) *reinterpret_cast<uint4 *>(sPlo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&bars[BB_PF0 + b]);
             }
             // ------------------------------------------------ dK, dV epilogue
             // Warpgroups 0, 1 store the two column halves of dK; 2, 3 of dV.
@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(800, 1)
                 if (!warp_wait(&bars[BB_DQF0 + qb], (it >> 1) & 1, abort, a.status)) break;
                 tc_fence_after();
                 uint32_t v[2][32];
-                tmem_ld32(tS0 + qb * 128 + lane_off, v[0]);
-                tmem_ld32(tS0 + qb * 128 + lane_off + 32, v[1]);
+                tmem_ld32(tdP0 + qb * 128 + lane_off, v[0]);
+                tmem_ld32(tdP0 + qb * 128 + lane_off + 32, v[1]);
                 tmem_ld_wait();
                 tmem_reg_fence(v[0]);
                 tmem_reg_fence(v[1]);
