@@ -32,7 +32,8 @@
 // Per half (M = 128 KV rows):
 //   S^T  = K Q^T        (SS, K-major/K-major)        -> TMEM
 //   dP^T = V dO^T       (SS, K-major/K-major)        -> TMEM
-//   P^T  = exp2(S^T * scale*log2e - lse*log2e),  dS^T = P^T o (dP^T - D)
+//   P^T  = exp2(S^T * scale*log2e - lse*log2e) as soon as S^T is written,
+//   dS^T = P^T o (dP^T - D) once dP^T is written (separate barriers)
 //          P^T written as bf16 into TMEM, dS^T into 128-byte-swizzled
 //          shared memory (precise mode: each as two bf16 terms hi + lo, ~16
 //          significant bits, both consumed by the MMAs below, so the
@@ -133,7 +134,7 @@ struct BwdSmem {
     static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
     static constexpr int kStat = kList + kListCap * 4;      // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
-    static constexpr int kNumBar = 24;
+    static constexpr int kNumBar = 26;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
@@ -141,7 +142,7 @@ struct BwdSmem {
 
 enum {
     BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_DF0, BB_DF1, BB_PF0, BB_PF1,
-    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1
+    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_SFD0, BB_SFD1
 };
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
@@ -212,8 +213,10 @@ __global__ void __launch_bounds__(800, 1)
                 mbar_init(&bars[BB_QF0 + s2], 33);
                 mbar_init(&bars[BB_QE0 + s2], 3);     // S^T, dP^T and dV/dK issuers
             }
-            mbar_init(&bars[BB_SF0], 2);      // S^T and dP^T issuers
-            mbar_init(&bars[BB_SF1], 2);
+            mbar_init(&bars[BB_SF0], 1);      // S^T written
+            mbar_init(&bars[BB_SF1], 1);
+            mbar_init(&bars[BB_SFD0], 1);     // dP^T written
+            mbar_init(&bars[BB_SFD1], 1);
             mbar_init(&bars[BB_DF0], 512);    // four P/dS warpgroups: dS^T written
             mbar_init(&bars[BB_DF1], 512);
             mbar_init(&bars[BB_PF0], 512);    // P^T written
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(800, 1)
                             const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
                             mma_ss(tD, sdesc_add(dA, ok_), sdesc_add(dB, oq), idS, kk > 0);
                         }
-                        tc_commit(&bars[BB_SF0 + b]);
+                        tc_commit(&bars[(role == 0 ? BB_SF0 : BB_SFD0) + b]);
                         tc_commit(&bars[BB_QE0 + st]);
                     } else {
                         const int qb = it & 1;         // score buffer: P^T in its S^T columns, dQ^T in its dP^T columns
@@ -429,12 +432,12 @@ __global__ void __launch_bounds__(800, 1)
                 const bool pred = ((entry(it >> 1) >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
                 const int st = it % NST;
                 const int b = it & 1;                     // score buffer
+                // P needs only S^T: dP^T is waited for after P^T has been handed to dV.
                 if (!warp_wait(&bars[BB_SF0 + b], (it >> 1) & 1, abort, a.status) ||
                     !warp_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sraw[CW], draw[CW];
                 tmem_ld16(tS0 + b * 128 + lane_off + c0, sraw);
-                tmem_ld16(tdP0 + b * 128 + lane_off + c0, draw);
                 // -lse*log2e and D of this warpgroup's columns, as packed pairs.
                 uint64_t nl2[CW / 2], dd2[CW / 2];
 #pragma unroll
@@ -446,7 +449,6 @@ __global__ void __launch_bounds__(800, 1)
                 }
                 tmem_ld_wait();
                 tmem_reg_fence(sraw);
-                tmem_reg_fence(draw);
                 // Column pairs in packed fp32: x = S*scale*log2e - lse*log2e,
                 // P = exp2(x), dS = P (dP - D).
                 float p[CW], ds[CW];
@@ -481,14 +483,19 @@ __global__ void __launch_bounds__(800, 1)
                     for (int w2 = 0; w2 < 8; ++w2) pw[w2] = pack_bf16x2(p[2 * w2], p[2 * w2 + 1]);
                     tmem_st8(tS0 + b * 128 + lane_off + c0, pw);
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars[BB_PF0 + b]);
+                if (!warp_wait(&bars[BB_SFD0 + b], (it >> 1) & 1, abort, a.status)) { ok = false; break; }
+                tc_fence_after();
+                tmem_ld16(tdP0 + b * 128 + lane_off + c0, draw);
+                tmem_ld_wait();
+                tmem_reg_fence(draw);
 #pragma unroll
                 for (int c = 0; c < CW; c += 2) {
                     const uint64_t t2 = f2_sub(f2_pack(__uint_as_float(draw[c]), __uint_as_float(draw[c + 1])), dd2[c / 2]);
                     f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]), t2), ds[c], ds[c + 1]);
                 }
-                tmem_st_wait();
-                tc_fence_before();
-                mbar_arrive(&bars[BB_PF0 + b]);
                 // dS^T (its buffer is free once dK, dQ^T of the half that last
                 // used it have completed, normally long ago), announced on DF.
                 const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;
