@@ -11,8 +11,7 @@
 // list of non-skip Q tiles of that KV tile (staged in shared memory), each as
 // two 64-row halves.
 //   warp 0      TMA producer (K and V once; Q, dO halves in a ring of three
-//               stages, two in precise mode; lse and D staged into shared
-//               memory by the whole warp)
+//               stages; lse and D staged into shared memory by the whole warp)
 //   warp 1      TMEM allocation; one thread issues the S^T MMAs
 //   warps 2-17  four warpgroups, one thread per KV row j each: P^T and dS^T
 //               for 16 of the half's 64 columns each
