@@ -47,8 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel, the hash of the source it was taken on (stale entries are ignored)
 # and the workload.
 NCU_TRAFFIC = {
-    ("bwd", "73d8dbdec0b7ebd5", "long_packing_128k"): 4311.90e6 + 2896.70e6,
-    ("bwd", "73d8dbdec0b7ebd5", "sliding_window"): 831.45e6 + 762.06e6,
+    ("bwd", "e51d130dcc45d28f", "long_packing_128k"): 4311.90e6 + 2896.70e6,
+    ("bwd", "e51d130dcc45d28f", "sliding_window"): 831.45e6 + 762.06e6,
 }
 
 

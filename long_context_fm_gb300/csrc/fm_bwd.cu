@@ -111,6 +111,11 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, v
 }
 
 // ---------------------------------------------------------------- main kernel
+enum {
+    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_DF0, BB_DF1, BB_PF0, BB_PF1,
+    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_SFD0, BB_SFD1, BB_COUNT
+};
+
 template <int D, bool PRECISE>
 struct BwdSmem {
     // Three Q/dO stages (a stage's next load is in flight while the two
@@ -133,16 +138,12 @@ struct BwdSmem {
     static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
     static constexpr int kStat = kList + kListCap * 4;      // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
-    static constexpr int kNumBar = 26;
+    static constexpr int kNumBar = BB_COUNT;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 + 1024 > 120 * 1024) ? kMisc + 64 + 1024 : 120 * 1024;
 };
 
-enum {
-    BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_DF0, BB_DF1, BB_PF0, BB_PF1,
-    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_SFD0, BB_SFD1
-};
 
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): the pair carries about
 // 16 significant bits, so products summed by the tensor core from both

@@ -46,6 +46,18 @@
 
 namespace fm {
 
+enum {
+    FB_Q = 0,
+    FB_KF0, FB_KF1, FB_KF2, FB_KE0, FB_KE1, FB_KE2,   // K stage loaded / released
+    FB_VF0, FB_VF1, FB_VE0, FB_VE1,                   // V stage loaded / released
+    FB_BF0, FB_BF1,                                   // bounds of the V stage's tile staged
+    FB_S0, FB_S1, FB_S2,                              // scores of buffer b computed
+    FB_P0, FB_P1, FB_P2,                              // P of buffer b written (both warpgroups)
+    FB_O0, FB_O1, FB_O2,                              // O += P V of a tile using buffer b completed
+    FB_DRAIN,                                         // every MMA of the CTA completed
+    FB_COUNT
+};
+
 template <int D, bool FP8 = false>
 struct FwdSmem {
     static constexpr int kBox = 128 * 128;        // one 128-byte wide, 128-row box (64 bf16 or 128 e4m3 columns)
@@ -60,22 +72,12 @@ struct FwdSmem {
     static constexpr int kListCap = 2048;                      // KV tiles staged from the plan
     static constexpr int kList = kSum + 2 * 128 * 4;
     static constexpr int kBar = kList + kListCap * 4;
-    static constexpr int kNumBar = 22;
+    static constexpr int kNumBar = FB_COUNT;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 > 120 * 1024) ? kMisc + 64 : 120 * 1024;
 };
 
-enum {
-    FB_Q = 0,
-    FB_KF0, FB_KF1, FB_KF2, FB_KE0, FB_KE1, FB_KE2,   // K stage loaded / released
-    FB_VF0, FB_VF1, FB_VE0, FB_VE1,                   // V stage loaded / released
-    FB_BF0, FB_BF1,                                   // bounds of the V stage's tile staged
-    FB_S0, FB_S1, FB_S2,                              // scores of buffer b computed
-    FB_P0, FB_P1, FB_P2,                              // P of buffer b written (both warpgroups)
-    FB_O0, FB_O1, FB_O2,                              // O += P V of a tile using buffer b completed
-    FB_DRAIN                                          // every MMA of the CTA completed
-};
 
 constexpr int kSB = 3;              // score buffers in TMEM
 constexpr int kSoftmaxBar = 1;      // named barrier of the two softmax warpgroups (256 threads)
