@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (t >= VS && !warp_wait(&bars[FB_VE0 + vs], ((t / VS) - 1) & 1, abort, a.status)) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bars[FB_VF0 + vs], S::kTile);
-#pragma unroll
+                    // V^T on the FP8 path, else the NBOX boxes of V
                     if (FP8)   // V^T tile: d rows x 128 key columns, [B*H][d][N] e4m3
                         tma_load_3d(smem + S::kV + vs * S::kTile, &tv, &bars[FB_VF0 + vs], kb, 0, bh);
                     else
