@@ -142,6 +142,38 @@ def total_pairs(wl, m):
     return tot
 
 
+def precision_flags(args, wl):
+    """FM_FLAG_PRECISE (1) or 0.  auto: precise for the x2-scaled prefix
+    workloads, whose gradients of tens exceed the max-abs bound with one bf16
+    rounding of P and dS (the mode their parity tests run in), standard for
+    every other workload."""
+    if args.precision == "auto":
+        return 1 if wl.input_scale != 1.0 else 0
+    return 1 if args.precision == "precise" else 0
+
+
+def hbm_bytes(wl, nnz_tiles, o_bytes=4, g_bytes=4):
+    """Algorithmic HBM bytes per launch of the memory-bound kernels: what each
+    must read and write at least once.
+      classify_minmax: 16 B of bounds per column read, 32 B of min/max per KV tile written
+      classify_lists:  the min/max read once; labels (1 B per tile pair), 4 B per
+                       non-skip pair in each of the two lists and 4 B per list count written
+      classify_order:  the list counts read, the two orders written
+      bwd_pre:         O and dO read, D (4 B per row) and the zeroed dQ accumulator written
+      bwd_post:        the dQ accumulator read, dQ written"""
+    S = wl.B * wl.Hm
+    n_t = -(-wl.N // 128)
+    rows = wl.B * wl.H * wl.N
+    d = wl.d
+    return {
+        "classify_minmax": S * (16 * wl.N + 32 * n_t),
+        "classify_lists": S * (32 * n_t + n_t * n_t + 8 * n_t) + 8 * nnz_tiles,
+        "classify_order": S * 16 * n_t,
+        "bwd_pre": rows * (o_bytes * d + 2 * d + 4 + 4 * d),
+        "bwd_post": rows * (4 * d + g_bytes * d),
+    }
+
+
 def max_over_ranks(vals, world, device):
     """Element-wise max of per-rank timings (the only collective of the run)."""
     t = torch.tensor(vals, dtype=torch.float64)
@@ -176,11 +208,18 @@ def run_fm(args, rank, world, local_rank):
     dq, dk, dv = (torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3))
     ws = torch.empty(fm.fm_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
     scale = wl.scale
+    flags = precision_flags(args, wl)
+    # non-skip (Q tile, KV tile) pairs: the classifier's list bytes
+    labels = torch.empty((B, wl.Hm, -(-N // 128), -(-N // 128)), dtype=torch.uint8, device=dev)
+    fm.fm_tile_classify(bounds, plan, status, labels=labels, stream=stream)
+    nnz_tiles = int(torch.count_nonzero(labels).item())
+    del labels
 
     def step():
         fm.fm_tile_classify(bounds, plan, status, stream=stream)
-        fm.fm_attn_fwd(q, k, v, bounds, plan, scale, o, lse, status, stream=stream)
-        fm.fm_attn_bwd(q, k, v, o, lse, dO, bounds, plan, scale, dq, dk, dv, ws, status, stream=stream)
+        fm.fm_attn_fwd(q, k, v, bounds, plan, scale, o, lse, status, stream=stream, flags=flags)
+        fm.fm_attn_bwd(q, k, v, o, lse, dO, bounds, plan, scale, dq, dk, dv, ws, status, stream=stream,
+                       flags=flags)
 
     def barrier():
         if world > 1:
@@ -216,7 +255,7 @@ def run_fm(args, rank, world, local_rank):
     launches = len(recs)
 
     # ---- the same step replayed from a captured graph (one launch per step)
-    gh = fm.fm_step_graph_create(q, k, v, dO, bounds, plan, scale, o, lse, status, dq, dk, dv, ws)
+    gh = fm.fm_step_graph_create(q, k, v, dO, bounds, plan, scale, o, lse, status, dq, dk, dv, ws, flags)
     for _ in range(2):
         fm.fm_step_graph_launch(gh, stream)
     torch.cuda.synchronize(dev)
@@ -319,9 +358,9 @@ def run_fm(args, rank, world, local_rank):
                 s_cmp.wait_event(ev_d2h[sidx])                   # the set's outputs have been read out
             fm.fm_tile_classify(bs["bounds"], plan, status, stream=s_cmp)
             fm.fm_attn_fwd(bs["q"], bs["k"], bs["v"], bs["bounds"], plan, scale, bs["o"], bs["lse"], status,
-                           stream=s_cmp)
+                           stream=s_cmp, flags=flags)
             fm.fm_attn_bwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["lse"], bs["dO"], bs["bounds"], plan, scale,
-                           bs["dq"], bs["dk"], bs["dv"], ws, status, stream=s_cmp)
+                           bs["dq"], bs["dk"], bs["dv"], ws, status, stream=s_cmp, flags=flags)
             ev_cmp[sidx].record(s_cmp)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(ev_cmp[sidx])
@@ -347,7 +386,7 @@ def run_fm(args, rank, world, local_rank):
     ms_step, e2e_s, graph_ms = max_over_ranks([ms_step, e2e_s, graph_ms], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
                 avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h,
-                graph_ms=graph_ms, fp8=fp8)
+                graph_ms=graph_ms, fp8=fp8, flags=flags, nnz_tiles=nnz_tiles)
 
 
 def mask_description(wl):
@@ -412,6 +451,9 @@ def main():
     ap.add_argument("--impl", default="fm", choices=["fm", "reference"])
     ap.add_argument("--config", default="long_packing_128k", choices=list(W.FULL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--precision", default="auto", choices=["auto", "standard", "precise"],
+                    help="standard: bf16 P and dS operands; precise: split-bf16 P and dS (FM_FLAG_PRECISE); "
+                         "auto: precise for the x2-scaled prefix workloads, standard otherwise")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -452,8 +494,24 @@ def main():
         bwd_tflops = r["bwd_flops"] / (bwd_ms * 1e-3) / 1e12
         peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         key = src_hash("fm_bwd.cu")
         traffic = NCU_TRAFFIC.get(("bwd", key, wl.name))
+        fwd_bwd_tflops = value / world
+
+        def fracs(x):
+            return {"burst": x / peak_burst, "sustained": x / peak_sus}
+
+        # The kernels are timed inside a step of a few milliseconds (a timed
+        # region well under a second): the burst peak is the one that applies;
+        # the sustained figure is given beside it.
+        hbm = {}
+        for kname, nbytes in hbm_bytes(wl, r["nnz_tiles"]).items():
+            ms = r["avg"].get(kname)
+            if ms:
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                hbm[kname] = {"bytes": nbytes, "ms": ms, "GB/s": gbs, "frac": gbs / peak_hbm}
+        precise = r["flags"] == 1
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_step"],
@@ -462,15 +520,19 @@ def main():
             "config": {"workload": r["wl"].name, "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
                        "mask": mask_description(wl),
                        "attended_pairs": r["pairs"], "outputs": "fp32 O, dQ, dK, dV",
-                       "precision": "standard (bf16 P and dS tensor-core operands, fp32 accumulation)",
+                       "precision": ("precise (split-bf16 P and dS tensor-core operands, fp32 accumulation)"
+                                     if precise else
+                                     "standard (bf16 P and dS tensor-core operands, fp32 accumulation)"),
                        "l2": l2_note(wl)},
             "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
-            "frac_of_peak": {"fwd": fwd_tflops / peak_burst, "fwd_bwd": value / world / peak_sus,
-                             "peaks": f"{src}: bf16 burst {peak_burst}, sustained {peak_sus}"},
+            "frac_of_peak": {"fwd": fracs(fwd_tflops), "bwd": fracs(bwd_tflops), "fwd_bwd": fracs(fwd_bwd_tflops),
+                             "peaks": f"{src}: bf16 burst {peak_burst}, sustained {peak_sus} TFLOP/s"},
             "kernel_ms": r["avg"],
+            "hbm": {"peak_GB/s": peak_hbm, "peak_source": f"{src} copy bandwidth", "kernels": hbm},
             "roofline": {"kernel": "fm_bwd_kernel", "bound": "tensor", "achieved": bwd_tflops,
-                         "peak": peak_sus, "unit": "TFLOP/s", "frac": bwd_tflops / peak_sus,
-                         "traffic": traffic, "peak_source": f"{src} bf16 sustained"},
+                         "peak": peak_burst, "unit": "TFLOP/s", "frac": bwd_tflops / peak_burst,
+                         "traffic": traffic, "peak_source": f"{src} bf16 burst",
+                         "frac_of_sustained": bwd_tflops / peak_sus},
             "gpu_launches": r["launches"],
             "fp8_fwd": None if r["fp8"] is None else {
                 "ms": r["fp8"][0], "value": world * r["fwd_flops"] / (r["fp8"][0] * 1e-3) / 1e12, "unit": "TFLOP/s",

@@ -212,9 +212,13 @@ FM_API fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const 
  * Limit: fm_bwd_workspace_bytes(B, H, N, d) <= FM_NOALLOC_SCRATCH_BYTES
  * (64 MiB: about 130,000 rows B*H*N at d = 128); larger sizes return
  * FM_ERR_WORKSPACE before anything is launched.
- * The first call made with a device current looks up the array's device
- * address on that device; make that first call before any stream capture.
+ * The first call made in a CUDA context (the device's primary context, or a
+ * context the caller made current) looks up the array's device address in
+ * that context; make that first call before any stream capture.  The lookup
+ * is cached per context id, so a context created later (after
+ * cudaDeviceReset, for example) gets a fresh lookup on its first call.
  * A device that has loaded the array keeps it until the process exits.
+ * Shape errors return the same codes as fm_attn_bwd.
  * Every call uses the same array: calls whose work overlaps on the GPU (for
  * example on two streams) race and give wrong results; calls ordered on one
  * stream are safe.  Each call clears what it needs; nothing carries over.

@@ -15,8 +15,8 @@ columns [s_r, s_{r+1}).  One step:
    tile labels of the row window skip every key tile, hence every key shard,
    that those rows never attend;
 4. backward for the rank's rows (``fm_attn_bwd_rows``): dQ is complete
-   locally; the dK, dV contributions of all ranks are summed (all-reduce) and
-   each rank keeps its own rows.
+   locally; the dK, dV contributions of all ranks are summed and scattered in
+   one reduce-scatter, so each rank receives only the sum over its own rows.
 
 The split ``balanced_splits`` is chosen before the data is distributed, from
 per-Q-tile costs (non-skip key tiles per Q tile, over batches and mask
@@ -24,7 +24,9 @@ heads): contiguous, 128-row aligned windows of nearly equal cost.
 
 The per-rank computation is a parameter (``LibraryLocal`` runs the CUDA
 library on the rank's GPU); the collectives come from ``torch.distributed``
-and run over NCCL or gloo alike.
+and run over NCCL or gloo alike.  A gloo group moves host tensors only, so
+with gloo the device tensors of a collective are staged through host copies
+(NCCL takes them as they are).
 """
 from __future__ import annotations
 
@@ -67,6 +69,12 @@ def split_costs(costs, splits, tile: int = TILE):
     return [float(costs[splits[r] // tile: -(-splits[r + 1] // tile)].sum()) for r in range(len(splits) - 1)]
 
 
+def _host_staged(group, t: torch.Tensor) -> bool:
+    """True when the group's backend moves host tensors only (gloo) and `t`
+    lives on a GPU: the collective then runs on a host copy."""
+    return t.is_cuda and dist.get_backend(group) == "gloo"
+
+
 def _gather_dim(local: torch.Tensor, splits, dim: int, group=None) -> torch.Tensor:
     """All-gather the per-rank slices of one axis (lengths from `splits`) into
     the full axis; pieces are padded to the longest so the collective sees
@@ -76,11 +84,35 @@ def _gather_dim(local: torch.Tensor, splits, dim: int, group=None) -> torch.Tens
     Lmax = max(lens)
     pad_shape = list(local.shape)
     pad_shape[dim] = Lmax
-    send = local.new_zeros(pad_shape)
+    staged = _host_staged(group, local)
+    send = local.new_zeros(pad_shape, device="cpu" if staged else local.device)
     send.narrow(dim, 0, local.shape[dim]).copy_(local)
     recv = [torch.empty_like(send) for _ in range(world)]
     dist.all_gather(recv, send, group=group)
-    return torch.cat([recv[r].narrow(dim, 0, lens[r]) for r in range(world)], dim=dim).contiguous()
+    out = torch.cat([recv[r].narrow(dim, 0, lens[r]) for r in range(world)], dim=dim).contiguous()
+    return out.to(local.device) if staged else out
+
+
+def reduce_scatter_rows(full: torch.Tensor, splits, rank: int, group=None) -> torch.Tensor:
+    """Sum the ranks' full-length contributions [B, H, N, d] and return this
+    rank's rows [B, H, L_r, d] of the sum: one reduce-scatter over pieces
+    padded to the longest window (each rank receives only its own rows)."""
+    world = len(splits) - 1
+    lens = [splits[r + 1] - splits[r] for r in range(world)]
+    Lmax = max(lens)
+    staged = _host_staged(group, full)
+    src = full.cpu() if staged else full
+    shape = list(full.shape)
+    shape[2] = Lmax
+    pieces = []
+    for r in range(world):
+        p = src.new_zeros(shape)
+        p.narrow(2, 0, lens[r]).copy_(src.narrow(2, splits[r], lens[r]))
+        pieces.append(p)
+    out = src.new_empty(shape)
+    dist.reduce_scatter(out, pieces, group=group)
+    out = out.narrow(2, 0, lens[rank]).contiguous()
+    return out.to(full.device) if staged else out
 
 
 def gather_bounds(local_bounds, splits, group=None):
@@ -151,7 +183,6 @@ def step(q, k, v, dO, local_bounds, splits, rank, scale, local, group=None):
     q_row0 = splits[rank]
     o, lse = local.forward(q, k_full, v_full, bounds, q_row0, scale)
     dq, dk_part, dv_part = local.backward(q, k_full, v_full, o, lse, dO, bounds, q_row0, scale)
-    dist.all_reduce(dk_part, group=group)
-    dist.all_reduce(dv_part, group=group)
-    r0, r1 = splits[rank], splits[rank + 1]
-    return o, lse, dq, dk_part[:, :, r0:r1].contiguous(), dv_part[:, :, r0:r1].contiguous()
+    dk = reduce_scatter_rows(dk_part, splits, rank, group)
+    dv = reduce_scatter_rows(dv_part, splits, rank, group)
+    return o, lse, dq, dk, dv

@@ -114,16 +114,6 @@ fm_status check_bounds(const fm_bounds &m, int B, int H, int N)
     return FM_OK;
 }
 
-fm_status check_shapes(int B, int H, int N, int d)
-{
-    if (B <= 0 || H <= 0 || N <= 0) return FM_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FM_ERR_UNSUPPORTED;
-    if (B > 65535 || H > 65535) return FM_ERR_UNSUPPORTED;
-    if ((int64_t)B * H * N * d > ((int64_t)1 << 40)) return FM_ERR_INVALID_ARG;
-    if ((int64_t)B * H > (1 << 30)) return FM_ERR_UNSUPPORTED;
-    return FM_OK;
-}
-
 // ---- profiler ------------------------------------------------------------------
 struct ProfRec {
     int kernel;
@@ -137,6 +127,16 @@ constexpr size_t kProfMax = 4096;
 }  // namespace
 
 namespace fm {
+fm_status check_shapes(int B, int H, int N, int d)
+{
+    if (B <= 0 || H <= 0 || N <= 0) return FM_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FM_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return FM_ERR_UNSUPPORTED;
+    if ((int64_t)B * H * N * d > ((int64_t)1 << 40)) return FM_ERR_INVALID_ARG;
+    if ((int64_t)B * H > (1 << 30)) return FM_ERR_UNSUPPORTED;
+    return FM_OK;
+}
+
 ProfScope::ProfScope(int kernel, void *st) : slot(-1), stream(st)
 {
     std::lock_guard<std::mutex> lk(g_prof_mu);

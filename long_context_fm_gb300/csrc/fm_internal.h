@@ -188,6 +188,11 @@ constexpr long long kWaitLimitCycles = 3000000000LL;
 
 // Host-side helpers implemented in fm_api.cu.
 namespace fm {
+// Shape checks shared by every attention entry point: FM_ERR_INVALID_ARG for
+// non-positive or overflowing sizes, FM_ERR_UNSUPPORTED for a head dim other
+// than 64 / 128 or B, H beyond the launch grid.
+fm_status check_shapes(int B, int H, int N, int d);
+
 struct ProfScope {
     // Records a start event on construction and a stop event on destruction
     // when profiling is on.

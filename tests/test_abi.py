@@ -309,3 +309,17 @@ def test_binding_fails_loudly_without_the_library():
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode != 0
     assert "ImportError" in r.stderr and "build" in r.stderr
+
+
+def test_noalloc_shape_errors_match_the_workspace_backward(fm):
+    """The allocation-free backward reports a bad shape with the same code as
+    fm_attn_bwd (both return before any CUDA call, so no GPU is needed)."""
+    import ctypes
+    cases = [(70000, 1, 256, 128), (1, 70000, 256, 128), (1, 1, 256, 96), (0, 1, 256, 128), (1, 1, -5, 64)]
+    for B, H, N, d in cases:
+        bounds = fm.Bounds(None, None, None, None, B, 1, N)
+        args = (None, None, None, None, 0, None, None, bounds, None, B, H, N, d, ctypes.c_float(0.1),
+                None, None, None, 1, 0)
+        want = fm._lib.fm_attn_bwd(*args, None, 0, None, None)
+        got = fm._lib.fm_attn_bwd_noalloc(*args, None, None)
+        assert got == want != fm.FM_OK, (B, H, N, d, got, want)

@@ -1,6 +1,9 @@
 """Row windows on the GPU (the per-rank computation of context parallelism),
-ranks emulated one after another on one device: each window's O and lse are
-the full call's rows bit for bit (a Q tile's list of key tiles does not
+ranks emulated one after another on one device: each window's O, lse and dQ
+match the oracle's rows of the whole mask, and the windows' dK, dV
+contributions summed match the oracle's gradients, within the parity
+tolerances; each window's O and lse are also the library's full call's rows
+bit for bit (a Q tile's list of key tiles does not
 depend on the window), dQ matches within the atomics' rounding, the dK, dV
 contributions of the windows add up to the full gradients, the window's tile
 labels are the oracle's rows, and key shards a window never attends get
@@ -40,6 +43,9 @@ def test_windows_reassemble_the_full_step(fm, name, world):
     bounds = [torch.from_numpy(np.ascontiguousarray(m[x])).cuda() for x in ("lts", "lte", "uts", "ute")]
     splits = cp.balanced_splits(_costs(m), wl.N, world)
     local = cp.LibraryLocal(flags)
+    qc, kc, vc, dOc = (t.cpu() for t in (q, k, v, dO))
+    O_ref, L_ref = oracle.forward(qc, kc, vc, m, wl.scale)
+    g_ref = oracle.backward(qc, kc, vc, dOc, m, wl.scale)
     dk_sum = torch.zeros(q.shape, dtype=torch.float32, device="cuda")
     dv_sum = torch.zeros_like(dk_sum)
     for r in range(world):
@@ -47,11 +53,18 @@ def test_windows_reassemble_the_full_step(fm, name, world):
         qs, dOs = q[:, :, r0:r1].contiguous(), dO[:, :, r0:r1].contiguous()
         o, lse = local.forward(qs, k, v, bounds, r0, wl.scale)
         dq, dk, dv = local.backward(qs, k, v, o, lse, dOs, bounds, r0, wl.scale)
+        # each window against the oracle's rows of the whole mask ...
+        check_all([(f"O window {r}", o.cpu().numpy(), O_ref[:, :, r0:r1]),
+                   ("lse", lse.cpu().numpy(), L_ref[:, :, r0:r1]),
+                   (f"dQ window {r}", dq.cpu().numpy(), g_ref["dq"][:, :, r0:r1])])
+        # ... and against the library's own whole-mask call
         assert torch.equal(o, full["o"][:, :, r0:r1]), r
         assert torch.equal(lse, full["lse"][:, :, r0:r1]), r
         torch.testing.assert_close(dq, full["dq"][:, :, r0:r1], rtol=1e-5, atol=1e-6)
         dk_sum += dk
         dv_sum += dv
+    check_all([("dK summed over windows", dk_sum.cpu().numpy(), g_ref["dk"]),
+               ("dV summed over windows", dv_sum.cpu().numpy(), g_ref["dv"])])
     torch.testing.assert_close(dk_sum, full["dk"], rtol=1e-5, atol=1e-5)
     torch.testing.assert_close(dv_sum, full["dv"], rtol=1e-5, atol=1e-5)
 
