@@ -33,6 +33,9 @@ fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                              const CUtensorMap &tdo, const BwdArgs &a, int d,
                              bool precise, cudaStream_t stream);
+fm_status fm_bwd128_prepare(int d);
+fm_status fm_bwd128_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                           const CUtensorMap &tdo, const BwdArgs &a, int d, cudaStream_t stream);
 
 namespace {
 
@@ -348,8 +351,11 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     if ((st = check_device()) != FM_OK) return st;
     CUtensorMap tq, tk, tv, tdo;
     float *dq_acc = reinterpret_cast<float *>(ws);
-    if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
-        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, 64))
+    // Standard mode walks whole 128-row Q tiles; precise mode 64-row halves.
+    const bool precise = (flags & FM_FLAG_PRECISE) != 0;
+    const int qrows = precise ? 64 : 128;
+    if (!make_tmap_bf16(&tq, q, B * H, Nq, d, qrows) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
+        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, qrows))
         return FM_ERR_CUDA;
     float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * Nq * d * 4));
     const int64_t rows = (int64_t)B * H * Nq;
@@ -364,8 +370,8 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     a.q_row0 = q_row0; a.Nq = Nq;
     a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.g_f32 = grad_dtype == FM_DT_F32;
-    if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
-        return st;
+    st = precise ? fm_bwd_main_launch(tq, tk, tv, tdo, a, d, true, s) : fm_bwd128_launch(tq, tk, tv, tdo, a, d, s);
+    if (st != FM_OK) return st;
     return fm_bwd_post_launch(dq_acc, dq, grad_dtype == FM_DT_F32, scale, rows * d, s);
 }
 
@@ -395,7 +401,7 @@ fm_status fm_step_graph_create(const fm_step_args *a, fm_step_graph *graph)
     if (a->d != 64 && a->d != 128) return FM_ERR_UNSUPPORTED;
     const bool precise = (a->flags & FM_FLAG_PRECISE) != 0;
     if ((st = fm_fwd_prepare(a->d, precise)) != FM_OK) return st;
-    if (a->dO && (st = fm_bwd_prepare(a->d, precise)) != FM_OK) return st;
+    if (a->dO && (st = (precise ? fm_bwd_prepare(a->d, true) : fm_bwd128_prepare(a->d))) != FM_OK) return st;
     cudaStream_t s = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return FM_ERR_CUDA;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
