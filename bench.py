@@ -142,6 +142,13 @@ def total_pairs(wl, m):
     return tot
 
 
+def workload_of(args):
+    """The named workload, with H overridden by --heads (a smaller case of the
+    same mask for profiler captures; the default run never sets it)."""
+    wl = W.FULL[args.config]
+    return wl.with_(H=args.heads) if args.heads else wl
+
+
 def precision_flags(args, wl):
     """FM_FLAG_PRECISE (1) or 0.  auto: precise for the x2-scaled prefix
     workloads, whose gradients of tens exceed the max-abs bound with one bf16
@@ -187,7 +194,7 @@ def max_over_ranks(vals, world, device):
 def run_fm(args, rank, world, local_rank):
     from long_context_fm_gb300 import fm
 
-    wl = W.FULL[args.config]
+    wl = workload_of(args)
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     m = W.make_mask(wl)
@@ -451,6 +458,8 @@ def main():
     ap.add_argument("--impl", default="fm", choices=["fm", "reference"])
     ap.add_argument("--config", default="long_packing_128k", choices=list(W.FULL))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="override the workload's head count (a smaller case of the same mask, for ncu captures)")
     ap.add_argument("--precision", default="auto", choices=["auto", "standard", "precise"],
                     help="standard: bf16 P and dS operands; precise: split-bf16 P and dS (FM_FLAG_PRECISE); "
                          "auto: precise for the x2-scaled prefix workloads, standard otherwise")
@@ -459,7 +468,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    wl = W.FULL[args.config]
+    wl = workload_of(args)
 
     if args.impl == "reference":
         if rank != 0:

@@ -179,7 +179,10 @@ FM_API fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bou
                       fm_stream_t stream);
 
 /* Workspace of fm_attn_bwd in bytes: fp32 dQ accumulator [B,H,N,d] plus
- * fp32 D = rowsum(dO * O) [B,H,N]. */
+ * fp32 D = rowsum(dO * O) [B,H,N].  (With fp32 gradients the kernels
+ * accumulate dQ in the caller's dq buffer directly and the accumulator
+ * part of the workspace is left untouched; the size is the same for both
+ * gradient dtypes.) */
 FM_API size_t fm_bwd_workspace_bytes(int B, int H, int N, int d);
 
 /*

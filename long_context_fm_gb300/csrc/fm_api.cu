@@ -21,8 +21,7 @@ fm_status fm_classify_launch(fm_bounds m, int q_row0, int Nq, int bq, int bk, vo
                              int32_t *status, cudaStream_t stream);
 fm_status fm_bwd_pre_launch(const void *o, int o_f32, const void *dO, float *Dout, float *dq_acc,
                             int64_t rows, int d, cudaStream_t stream);
-fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,
-                             cudaStream_t stream);
+fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, float scale, int64_t n, cudaStream_t stream);
 fm_status fm_fwd_prepare(int d, bool precise);
 fm_status fm_fwd_prepare_fp8();
 fm_status fm_fwd_launch_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
@@ -33,9 +32,6 @@ fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                              const CUtensorMap &tdo, const BwdArgs &a, int d,
                              bool precise, cudaStream_t stream);
-fm_status fm_bwd128_prepare(int d);
-fm_status fm_bwd128_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                           const CUtensorMap &tdo, const BwdArgs &a, int d, cudaStream_t stream);
 
 namespace {
 
@@ -351,28 +347,31 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     if ((st = check_device()) != FM_OK) return st;
     CUtensorMap tq, tk, tv, tdo;
     float *dq_acc = reinterpret_cast<float *>(ws);
-    // Standard mode walks whole 128-row Q tiles; precise mode 64-row halves.
-    const bool precise = (flags & FM_FLAG_PRECISE) != 0;
-    const int qrows = precise ? 64 : 128;
-    if (!make_tmap_bf16(&tq, q, B * H, Nq, d, qrows) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
-        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, qrows))
+    if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
+        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, 64))
         return FM_ERR_CUDA;
     float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * Nq * d * 4));
     const int64_t rows = (int64_t)B * H * Nq;
     cudaStream_t s = (cudaStream_t)stream;
+    // fp32 gradients: dQ is accumulated (already scaled) in the caller's dq,
+    // so no postprocess pass; bf16 gradients: unscaled in the workspace, then
+    // scaled and converted by the postprocess.
+    const bool dq_direct = grad_dtype == FM_DT_F32;
+    if (dq_direct) dq_acc = reinterpret_cast<float *>(dq);
     if ((st = fm_bwd_pre_launch(o, o_dtype == FM_DT_F32, dO, Dvec, dq_acc, rows, d, s)) != FM_OK) return st;
     BwdArgs a;
     a.lts = m.lts; a.lte = m.lte; a.uts = m.uts; a.ute = m.ute;
     a.plan = (const uint8_t *)plan; a.L = L;
     a.lse = lse; a.Dvec = Dvec; a.dq_acc = dq_acc;
+    a.dq_mul = dq_direct ? scale : 1.f;
     a.dk = dk; a.dv = dv; a.status = dev_status;
     a.B = B; a.H = H; a.Hm = m.Hm; a.N = N;
     a.q_row0 = q_row0; a.Nq = Nq;
     a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.g_f32 = grad_dtype == FM_DT_F32;
-    st = precise ? fm_bwd_main_launch(tq, tk, tv, tdo, a, d, true, s) : fm_bwd128_launch(tq, tk, tv, tdo, a, d, s);
-    if (st != FM_OK) return st;
-    return fm_bwd_post_launch(dq_acc, dq, grad_dtype == FM_DT_F32, scale, rows * d, s);
+    if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
+        return st;
+    return dq_direct ? FM_OK : fm_bwd_post_launch(dq_acc, dq, scale, rows * d, s);
 }
 
 fm_status fm_attn_bwd(const void *q, const void *k, const void *v, const void *o, int o_dtype,
@@ -401,7 +400,7 @@ fm_status fm_step_graph_create(const fm_step_args *a, fm_step_graph *graph)
     if (a->d != 64 && a->d != 128) return FM_ERR_UNSUPPORTED;
     const bool precise = (a->flags & FM_FLAG_PRECISE) != 0;
     if ((st = fm_fwd_prepare(a->d, precise)) != FM_OK) return st;
-    if (a->dO && (st = (precise ? fm_bwd_prepare(a->d, true) : fm_bwd128_prepare(a->d))) != FM_OK) return st;
+    if (a->dO && (st = fm_bwd_prepare(a->d, precise)) != FM_OK) return st;
     cudaStream_t s = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return FM_ERR_CUDA;
     if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {

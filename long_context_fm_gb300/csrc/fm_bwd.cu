@@ -16,7 +16,9 @@
 //   warps 2-17  four warpgroups, one thread per KV row j each: P^T and dS^T
 //               for 16 of the half's 64 columns each
 //   warps 18-21 one thread per head-dim index: drain dQ^T from TMEM into the
-//               fp32 dQ accumulator with red.global.add
+//               fp32 dQ accumulator with red.global.add (the caller's fp32 dQ,
+//               scaled on the way, or the workspace accumulator that the
+//               postprocess scales and converts to bf16)
 //   warp 22     one thread issues the dQ^T MMAs
 //   warp 23     one thread issues the dP^T MMAs
 //   warp 24     one thread issues the dV, then dK MMAs
@@ -92,21 +94,19 @@ __global__ void __launch_bounds__(256) fm_bwd_pre_kernel(const void *o, int o_f3
 }
 
 // ---------------------------------------------------------------- postprocess
-// dQ = scale * dQacc, converted to the gradient dtype.  4 elements per thread.
-__global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, void *dq, int g_f32,
-                                                          float scale, int64_t n4)
+// bf16 gradients: dQ = scale * dQacc, rounded to bf16.  4 elements per thread.
+// (fp32 gradients need no postprocess: the main kernel adds scale * dQ^T into
+// the caller's buffer directly.)
+__global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, uint16_t *dq, float scale,
+                                                          int64_t n4)
 {
     for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4;
          t += (int64_t)gridDim.x * blockDim.x) {
         const float4 x = reinterpret_cast<const float4 *>(dq_acc)[t];
-        if (g_f32) {
-            reinterpret_cast<float4 *>(dq)[t] = make_float4(x.x * scale, x.y * scale, x.z * scale, x.w * scale);
-        } else {
-            uint2 w;
-            w.x = pack_bf16x2(x.x * scale, x.y * scale);
-            w.y = pack_bf16x2(x.z * scale, x.w * scale);
-            reinterpret_cast<uint2 *>(dq)[t] = w;
-        }
+        uint2 w;
+        w.x = pack_bf16x2(x.x * scale, x.y * scale);
+        w.y = pack_bf16x2(x.z * scale, x.w * scale);
+        reinterpret_cast<uint2 *>(dq)[t] = w;
     }
 }
 
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(800, 1)
                 const int lim = min(64, Nq - q0);      // rows beyond the Q rows: nothing to add
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
-                    if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]));
+                    if (c < lim) red_add_f32(dst + (int64_t)c * D, __uint_as_float(v[c >> 5][c & 31]) * a.dq_mul);
             }
         }
     }
@@ -671,14 +671,13 @@ fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const
                    : launch_bwd<64, false>(tq, tk, tv, tdo, a, stream);
 }
 
-fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, int g_f32, float scale, int64_t n,
-                             cudaStream_t stream)
+fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, float scale, int64_t n, cudaStream_t stream)
 {
     const int64_t n4 = n / 4;
     int64_t blocks = (n4 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
     ProfScope ps(kKBwdPost, stream);
-    fm_bwd_post_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, dq, g_f32, scale, n4);
+    fm_bwd_post_kernel<<<(unsigned)blocks, 256, 0, stream>>>(dq_acc, reinterpret_cast<uint16_t *>(dq), scale, n4);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }

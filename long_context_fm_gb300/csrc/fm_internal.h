@@ -155,7 +155,8 @@ struct BwdArgs {
     PlanLayout L;
     const float *lse;     // forward logsumexp, natural log
     const float *Dvec;    // rowsum(dO * O)
-    float *dq_acc;        // fp32 dQ accumulator (unscaled)
+    float *dq_acc;        // fp32 dQ accumulator: the caller's dq (fp32 gradients) or the workspace
+    float dq_mul;         // factor of the accumulated dQ^T: scale (caller's dq) or 1 (workspace, scaled later)
     void *dk, *dv;
     int32_t *status;
     int B, H, Hm, N;

@@ -187,13 +187,16 @@ def test_bounded_wait_times_out_and_context_survives(fm):
 
 
 def test_profiler_records_every_launch(fm):
+    """Every launch of a step, in order; fp32 gradients accumulate dQ in the
+    caller's buffer directly (no postprocess), bf16 gradients go through the
+    postprocess that scales and rounds the accumulator."""
     wl = W.SMALL["docs_small"]
     m = W.make_mask(wl)
     q, k, v, dO = W.make_inputs(wl)
-    fm.fm_profile_begin()
-    run_fm(fm, wl, m, q, k, v, dO)
-    rec = fm.fm_profile_end()
-    names = [r[0] for r in rec]
-    assert names == ["classify_minmax", "classify_lists", "classify_order", "fwd", "bwd_pre", "bwd",
-                     "bwd_post"]
-    assert all(ms > 0 for _, ms in rec)
+    head = ["classify_minmax", "classify_lists", "classify_order", "fwd", "bwd_pre", "bwd"]
+    for g_dtype, tail in ((torch.float32, []), (torch.bfloat16, ["bwd_post"])):
+        fm.fm_profile_begin()
+        run_fm(fm, wl, m, q, k, v, dO, g_dtype=g_dtype)
+        rec = fm.fm_profile_end()
+        assert [r[0] for r in rec] == head + tail, g_dtype
+        assert all(ms > 0 for _, ms in rec)
