@@ -346,6 +346,23 @@ FM_API fm_status fm_profile_begin(void);
 FM_API int fm_profile_end(fm_kernel_time *out, int max_entries);
 
 /*
+ * fm_debug_wait_test — HOST, test hook; nothing calls it in a product path.
+ * Failure detection is tested on the real kernels without faulting the GPU:
+ * after this call, the next fm_attn_fwd / fm_attn_fwd_rows launch
+ * (kernel = 0) or fm_attn_bwd / fm_attn_bwd_rows launch (kernel = 1) made by
+ * the process bounds every device-side wait by limit_cycles SM cycles
+ * (100,000 .. the default bound of about 3e9) instead of the default, and
+ * its first CTA withholds the load of its second K tile (forward) or of its
+ * second Q/dO half (backward).  The wait for that load runs out: the kernel
+ * writes FM_ERR_TIMEOUT to dev_status, raises its abort flag (every other
+ * wait of the CTA then gives up), drains the copies and tensor-core products
+ * it issued, frees its TMEM and returns; the CUDA context stays usable.
+ * The switch is consumed by that one launch; kernel = -1 clears it.
+ * Returns FM_ERR_INVALID_ARG for another kernel id or a limit out of range.
+ */
+FM_API fm_status fm_debug_wait_test(int kernel, long long limit_cycles);
+
+/*
  * Self-test of the bounded wait used by every pipeline barrier: one CTA
  * waits on a barrier that nothing completes, gives up after about
  * limit_cycles SM clock cycles and writes FM_ERR_TIMEOUT to dev_status.

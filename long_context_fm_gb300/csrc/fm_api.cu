@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -111,6 +112,25 @@ fm_status check_bounds(const fm_bounds &m, int B, int H, int N)
         return FM_ERR_INVALID_ARG;
     if (m.B != B || m.N != N || !(m.Hm == 1 || m.Hm == H)) return FM_ERR_INVALID_ARG;
     return FM_OK;
+}
+
+// ---- wait test hook --------------------------------------------------------------
+// One-shot, set only by fm_debug_wait_test: the next forward (kernel 0) or
+// backward main (kernel 1) launch runs with a short wait bound and its first
+// CTA withholds one tile load.
+std::atomic<int> g_dbg_kernel{-1};
+std::atomic<long long> g_dbg_limit{0};
+
+void wait_test_args(int kernel, long long *limit, int *withhold)
+{
+    *limit = kWaitLimitCycles;
+    *withhold = 0;
+    int want = kernel;
+    if (g_dbg_kernel.load(std::memory_order_acquire) == kernel &&
+        g_dbg_kernel.compare_exchange_strong(want, -1, std::memory_order_acq_rel)) {
+        *limit = g_dbg_limit.load(std::memory_order_acquire);
+        *withhold = 1;
+    }
 }
 
 // ---- profiler ------------------------------------------------------------------
@@ -268,6 +288,7 @@ fm_status fm_attn_fwd_rows(const void *q, const void *k, const void *v, fm_bound
     a.scale_log2 = scale * 1.4426950408889634f;
     a.o_f32 = o_dtype == FM_DT_F32;
     a.descale = nullptr;
+    wait_test_args(0, &a.wait_limit, &a.withhold);
     return fm_fwd_launch(tq, tk, tv, a, d, (flags & FM_FLAG_PRECISE) != 0, (cudaStream_t)stream);
 }
 
@@ -302,6 +323,8 @@ fm_status fm_attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v
     a.scale_log2 = scale * 1.4426950408889634f;
     a.o_f32 = o_dtype == FM_DT_F32;
     a.descale = descale;
+    a.wait_limit = kWaitLimitCycles;
+    a.withhold = 0;
     return fm_fwd_launch_fp8(tq, tk, tvt, a, (cudaStream_t)stream);
 }
 
@@ -369,6 +392,7 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     a.q_row0 = q_row0; a.Nq = Nq;
     a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.g_f32 = grad_dtype == FM_DT_F32;
+    wait_test_args(1, &a.wait_limit, &a.withhold);
     if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
         return st;
     return dq_direct ? FM_OK : fm_bwd_post_launch(dq_acc, dq, scale, rows * d, s);
@@ -483,6 +507,16 @@ int fm_profile_end(fm_kernel_time *out, int max_entries)
     }
     g_prof.clear();
     return err ? -1 : n;
+}
+
+fm_status fm_debug_wait_test(int kernel, long long limit_cycles)
+{
+    if ((kernel != 0 && kernel != 1 && kernel != -1) || (kernel >= 0 && (limit_cycles < 100000 ||
+                                                                        limit_cycles > kWaitLimitCycles)))
+        return FM_ERR_INVALID_ARG;
+    g_dbg_limit.store(limit_cycles, std::memory_order_release);
+    g_dbg_kernel.store(kernel, std::memory_order_release);
+    return FM_OK;
 }
 
 fm_status fm_selftest_wait_timeout(long long limit_cycles, int32_t *dev_status, fm_stream_t stream)

@@ -188,11 +188,14 @@ __global__ void __launch_bounds__(384, 1)
                     tma_load_3d(smem + S::kQ + x * S::kBox, &tq, &bars[FB_Q], x * BOXW, qt * 128, bh);
             }
             int nk = 0;   // K loads issued
+            // Test hook: the first CTA withholds the K load of its second tile,
+            // so that the scores' wait for it runs out (never set by a product call).
+            const int withheld = (a.withhold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? 1 : -1;
             for (int t = 0; t < n; ++t) {
                 const int kb = (entry(t) & kTileMask) * 128;
                 const int ks = t % KS;
-                if (t >= KS && !warp_wait(&bars[FB_KE0 + ks], ((t / KS) - 1) & 1, abort, a.status)) break;
-                if (lane == 0) {
+                if (t >= KS && !warp_wait(&bars[FB_KE0 + ks], ((t / KS) - 1) & 1, abort, a.status, a.wait_limit)) break;
+                if (lane == 0 && t != withheld) {
                     mbar_arrive_expect_tx(&bars[FB_KF0 + ks], S::kTile);
 #pragma unroll
                     for (int x = 0; x < NBOX; ++x)
@@ -202,9 +205,9 @@ __global__ void __launch_bounds__(384, 1)
             }
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
-                if (n > 0) mbar_wait_drain(&bars[FB_Q], 0, a.status);
+                if (n > 0) mbar_wait_drain(&bars[FB_Q], 0, a.status, a.wait_limit);
                 for (int k2 = (nk > KS ? nk - KS : 0); k2 < nk; ++k2)
-                    mbar_wait_drain(&bars[FB_KF0 + (k2 % KS)], (k2 / KS) & 1, a.status);
+                    if (k2 != withheld) mbar_wait_drain(&bars[FB_KF0 + (k2 % KS)], (k2 / KS) & 1, a.status, a.wait_limit);
             }
         } else if (warp == 10) {
             // ------------------------------------------------ V producer
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(384, 1)
                         }
                     }
                 }
-                if (t >= VS && !warp_wait(&bars[FB_VE0 + vs], ((t / VS) - 1) & 1, abort, a.status)) break;
+                if (t >= VS && !warp_wait(&bars[FB_VE0 + vs], ((t / VS) - 1) & 1, abort, a.status, a.wait_limit)) break;
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&bars[FB_VF0 + vs], S::kTile);
                     // V^T on the FP8 path, else the NBOX boxes of V
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (lane == 0 && *abort)
                 for (int k2 = (nv > VS ? nv - VS : 0); k2 < nv; ++k2)
-                    mbar_wait_drain(&bars[FB_VF0 + (k2 % VS)], (k2 / VS) & 1, a.status);
+                    mbar_wait_drain(&bars[FB_VF0 + (k2 % VS)], (k2 / VS) & 1, a.status, a.wait_limit);
         } else if (warp == 1) {
             // ------------------------------------------------ S issuer
             // The scores of tile t as soon as its K has landed and its score buffer
@@ -266,12 +269,12 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0 && n > 0) {
                 constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
                 const uint64_t dQ = sdesc_sw128(smem_u32(smem + S::kQ), 16, 1024);
-                bool ok = mbar_wait(&bars[FB_Q], 0, abort, a.status);
+                bool ok = mbar_wait(&bars[FB_Q], 0, abort, a.status, a.wait_limit);
                 for (int t = 0; ok && t < n; ++t) {
                     const int ks = t % KS;
-                    if (!mbar_wait(&bars[FB_KF0 + ks], (t / KS) & 1, abort, a.status)) break;
+                    if (!mbar_wait(&bars[FB_KF0 + ks], (t / KS) & 1, abort, a.status, a.wait_limit)) break;
                     // The buffer's previous tile, t - 3, must have finished its PV.
-                    if (t >= kSB && !mbar_wait(&bars[FB_O0 + t % kSB], ((t - kSB) / kSB) & 1, abort, a.status)) break;
+                    if (t >= kSB && !mbar_wait(&bars[FB_O0 + t % kSB], ((t - kSB) / kSB) & 1, abort, a.status, a.wait_limit)) break;
                     tc_fence_after();
                     const uint64_t dK = sdesc_sw128(smem_u32(smem + S::kK + ks * S::kTile), 16, 1024);
                     const uint32_t tS = tmem + (t % kSB) * 128;
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(384, 1)
             if (lane == 0) {
                 // Every MMA of this CTA (both issuers) completes before TMEM is released.
                 tc_commit(&bars[FB_DRAIN]);
-                mbar_wait_drain(&bars[FB_DRAIN], 0, a.status);
+                mbar_wait_drain(&bars[FB_DRAIN], 0, a.status, a.wait_limit);
             }
         } else if (warp == 11) {
             // ------------------------------------------------ PV issuer
@@ -304,8 +307,8 @@ __global__ void __launch_bounds__(384, 1)
                 const uint32_t tO = tmem + 384;
                 for (int t = 0; t < n; ++t) {
                     const int vs = t % VS;
-                    if (!mbar_wait(&bars[FB_VF0 + vs], (t / VS) & 1, abort, a.status) ||
-                        !mbar_wait(&bars[FB_P0 + t % kSB], (t / kSB) & 1, abort, a.status))
+                    if (!mbar_wait(&bars[FB_VF0 + vs], (t / VS) & 1, abort, a.status, a.wait_limit) ||
+                        !mbar_wait(&bars[FB_P0 + t % kSB], (t / kSB) & 1, abort, a.status, a.wait_limit))
                         break;
                     tc_fence_after();
                     const uint32_t tP = tmem + (t % kSB) * 128;
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(384, 1)
             }
             if (lane == 0) {
                 tc_commit(&bars[FB_DRAIN]);
-                mbar_wait_drain(&bars[FB_DRAIN], 0, a.status);
+                mbar_wait_drain(&bars[FB_DRAIN], 0, a.status, a.wait_limit);
             }
         } else {
             // ------------------------------------------------ softmax (warps 2-9)
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(384, 1)
             bool live = true;
             // The PV of tile k has completed (and with it every earlier MMA).
             auto wait_pv = [&](int k) {
-                live = live && warp_wait(&bars[FB_O0 + k % kSB], (k / kSB) & 1, abort, a.status);
+                live = live && warp_wait(&bars[FB_O0 + k % kSB], (k / kSB) & 1, abort, a.status, a.wait_limit);
             };
             for (int t = 0; t < n; ++t) {
                 const int e = entry(t);
@@ -359,8 +362,8 @@ __global__ void __launch_bounds__(384, 1)
                 const bool pred = ((e >> kLabelShift) == FM_TILE_PARTIAL) || kb + 128 > N;
                 const int bb = t % kSB, vs = t % VS;
                 const uint32_t tS = tmem + bb * 128;
-                live = live && warp_wait(&bars[FB_S0 + bb], (t / kSB) & 1, abort, a.status);
-                live = live && (!pred || warp_wait(&bars[FB_BF0 + vs], (t / VS) & 1, abort, a.status));
+                live = live && warp_wait(&bars[FB_S0 + bb], (t / kSB) & 1, abort, a.status, a.wait_limit);
+                live = live && (!pred || warp_wait(&bars[FB_BF0 + vs], (t / VS) & 1, abort, a.status, a.wait_limit));
                 float sv[64];
                 float mxl = -INFINITY;
                 if (live) {

@@ -146,6 +146,8 @@ struct FwdArgs {
     float scale_log2;     // softmax scale * log2(e)
     int o_f32;
     const float *descale; // FP8 path: device [3], the Q, K, V descales (else unused)
+    long long wait_limit; // bound of every device-side wait, SM cycles (kWaitLimitCycles)
+    int withhold;         // test hook (0 in every product launch): CTA 0 skips its second K load
 };
 
 // Arguments of the backward main kernel.
@@ -163,6 +165,8 @@ struct BwdArgs {
     int q_row0, Nq;       // Q, dO, lse, D, dQ hold rows [q_row0, q_row0 + Nq); K, V, dK, dV all N
     float scale, scale_log2;
     int g_f32;
+    long long wait_limit; // bound of every device-side wait, SM cycles (kWaitLimitCycles)
+    int withhold;         // test hook (0 in every product launch): CTA 0 skips its second Q/dO load
 };
 
 // Kernel ids for the profiler.

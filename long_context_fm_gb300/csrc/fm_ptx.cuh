@@ -139,9 +139,9 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
 // all lanes saw the phase complete, so .sync.aligned instructions that follow
 // are executed by the whole warp or by none of it.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int32_t *status)
+                                          int32_t *status, long long limit = kWaitLimitCycles)
 {
-    const bool ok = mbar_wait(bar, parity, abort, status);
+    const bool ok = mbar_wait(bar, parity, abort, status, limit);
     return __all_sync(0xffffffffu, ok);
 }
 

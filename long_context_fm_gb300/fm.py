@@ -31,7 +31,7 @@ EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_mask_
             "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
             "fm_attn_bwd_noalloc", "fm_step_graph_create", "fm_step_graph_launch", "fm_step_graph_destroy",
             "fm_plan_bytes_rows", "fm_tile_classify_rows", "fm_attn_fwd_rows", "fm_attn_bwd_rows",
-            "fm_quantize_fp8", "fm_attn_fwd_fp8"]
+            "fm_quantize_fp8", "fm_attn_fwd_fp8", "fm_debug_wait_test"]
 # Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -86,6 +86,7 @@ _lib.fm_profile_begin.argtypes = []
 _lib.fm_profile_end.restype = _I
 _lib.fm_profile_end.argtypes = [_P, _I]
 _lib.fm_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _P, _P]
+_lib.fm_debug_wait_test.argtypes = [ctypes.c_int, ctypes.c_longlong]
 _lib.fm_plan_bytes_rows.restype = _SZ
 _lib.fm_plan_bytes_rows.argtypes = [_I, _I, _I, _I, _I, _I, _I]
 _lib.fm_tile_classify_rows.argtypes = [Bounds, _I, _I, _I, _I, _P, _SZ, _P, _P, _P]
@@ -272,6 +273,13 @@ def fm_profile_end(max_entries=4096):
     if n < 0:
         raise FmError(FM_ERR_CUDA, "fm_profile_end")
     return [(KERNEL_NAMES[buf[i].kernel], float(buf[i].ms)) for i in range(n)]
+
+
+def fm_debug_wait_test(kernel, limit_cycles):
+    """Test hook: the next forward (kernel=0) or backward (kernel=1) launch runs
+    with every device-side wait bounded by limit_cycles and its first CTA
+    withholds one tile load, so it must end with FM_ERR_TIMEOUT in dev_status."""
+    _check(_lib.fm_debug_wait_test(int(kernel), int(limit_cycles)), "fm_debug_wait_test")
 
 
 def fm_selftest_wait_timeout(limit_cycles, dev_status, stream=None):

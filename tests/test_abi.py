@@ -287,6 +287,14 @@ def test_interval_converter_rejects_bad_input(fm):
     assert fm._lib.fm_mask_from_row_intervals(None, p, 1, 1, 1, 2, p, p, p, p) == fm.FM_ERR_INVALID_ARG
 
 
+def test_wait_test_hook_argument_checks(fm):
+    """The test hook rejects unknown kernels and out-of-range bounds; -1 clears it."""
+    assert fm._lib.fm_debug_wait_test(2, 1_000_000) == fm.FM_ERR_INVALID_ARG
+    assert fm._lib.fm_debug_wait_test(0, 10) == fm.FM_ERR_INVALID_ARG
+    assert fm._lib.fm_debug_wait_test(1, 10**12) == fm.FM_ERR_INVALID_ARG
+    assert fm._lib.fm_debug_wait_test(-1, 0) == fm.FM_OK
+
+
 def test_step_graph_null_arguments(fm):
     """Argument checks that need no GPU: no graph handle or no arguments."""
     import ctypes

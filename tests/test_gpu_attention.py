@@ -186,6 +186,46 @@ def test_bounded_wait_times_out_and_context_survives(fm):
     check_close("O", out["o"].cpu().numpy(), O)
 
 
+@pytest.mark.parametrize("kernel", ["forward", "backward"])
+def test_real_kernel_wait_runs_out_and_context_survives(fm, kernel):
+    """The real attention kernel's abort path: with the test hook armed, the
+    first CTA of the launch withholds one tile load, the wait for it runs out
+    after 2e6 cycles, the kernel reports FM_ERR_TIMEOUT (its other waits give
+    up on the abort flag, it drains its copies and products and frees TMEM),
+    and the context then still passes a parity case."""
+    wl = W.Workload("unmasked_512", B=1, H=2, N=512, d=128, mask="full")   # every list has 4 tiles
+    m = W.make_mask(wl)
+    q, k, v, dO = (t.cuda() for t in W.make_inputs(wl))
+    att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"])
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    fm.fm_attn_fwd(q, k, v, att.bounds, att.plan, wl.scale, o, lse, att.status)
+    torch.cuda.synchronize()
+    assert int(att.status.item()) == 0
+    g = [torch.empty(q.shape, dtype=torch.float32, device="cuda") for _ in range(3)]
+    ws = torch.empty(fm.fm_bwd_workspace_bytes(*q.shape), dtype=torch.uint8, device="cuda")
+    fm.fm_debug_wait_test(0 if kernel == "forward" else 1, 2_000_000)
+    try:
+        if kernel == "forward":
+            fm.fm_attn_fwd(q, k, v, att.bounds, att.plan, wl.scale, o, lse, att.status)
+        else:
+            fm.fm_attn_bwd(q, k, v, o, lse, dO, att.bounds, att.plan, wl.scale, *g, ws, att.status)
+        torch.cuda.synchronize()
+    finally:
+        fm.fm_debug_wait_test(-1, 0)
+    assert int(att.status.item()) == fm.FM_ERR_TIMEOUT
+    # the switch was consumed by that one launch; the context still works
+    small = W.SMALL["docs_small"]
+    ms = W.make_mask(small)
+    qs, ks, vs, dOs = W.make_inputs(small)
+    out = run_fm(fm, small, ms, qs, ks, vs, dOs)
+    O, L = oracle.forward(qs, ks, vs, ms, small.scale)
+    gr = oracle.backward(qs, ks, vs, dOs, ms, small.scale)
+    check_all([("O", out["o"].cpu().numpy(), O), ("lse", out["lse"].cpu().numpy(), L),
+               ("dQ", out["dq"].cpu().numpy(), gr["dq"]), ("dK", out["dk"].cpu().numpy(), gr["dk"]),
+               ("dV", out["dv"].cpu().numpy(), gr["dv"])])
+
+
 def test_profiler_records_every_launch(fm):
     """Every launch of a step, in order; fp32 gradients accumulate dQ in the
     caller's buffer directly (no postprocess), bf16 gradients go through the
