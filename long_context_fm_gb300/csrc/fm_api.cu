@@ -146,6 +146,18 @@ constexpr size_t kProfMax = 4096;
 }  // namespace
 
 namespace fm {
+int device_sm_count()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int v = cached[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
+    cached[dev].store(v, std::memory_order_release);
+    return v;
+}
+
 fm_status check_shapes(int B, int H, int N, int d)
 {
     if (B <= 0 || H <= 0 || N <= 0) return FM_ERR_INVALID_ARG;

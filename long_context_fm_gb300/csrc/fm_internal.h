@@ -148,6 +148,7 @@ struct FwdArgs {
     const float *descale; // FP8 path: device [3], the Q, K, V descales (else unused)
     long long wait_limit; // bound of every device-side wait, SM cycles (kWaitLimitCycles)
     int withhold;         // test hook (0 in every product launch): CTA 0 skips its second K load
+    int sched_slot;       // work-counter slot of this launch (persistent scheduling)
 };
 
 // Arguments of the backward main kernel.
@@ -193,6 +194,10 @@ constexpr long long kWaitLimitCycles = 3000000000LL;
 
 // Host-side helpers implemented in fm_api.cu.
 namespace fm {
+// Number of SMs of the current device (cached per device; 0 on error): the
+// grid of the persistent attention kernels.
+int device_sm_count();
+
 // Shape checks shared by every attention entry point: FM_ERR_INVALID_ARG for
 // non-positive or overflowing sizes, FM_ERR_UNSUPPORTED for a head dim other
 // than 64 / 128 or B, H beyond the launch grid.
