@@ -113,8 +113,22 @@ __global__ void __launch_bounds__(256) fm_bwd_post_kernel(const float *dq_acc, u
 // ---------------------------------------------------------------- main kernel
 enum {
     BB_KV = 0, BB_QF0, BB_QF1, BB_QF2, BB_QE0, BB_QE1, BB_QE2, BB_SF0, BB_SF1, BB_DF0, BB_DF1, BB_PF0, BB_PF1,
-    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_SFD0, BB_SFD1, BB_COUNT
+    BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_SFD0, BB_SFD1,
+    BB_KVE,                                   // the unit's S^T, dP^T and dQ^T have read K and V
+    BB_ACCE,                                  // the unit's epilogue has read dK and dV
+    BB_UF0, BB_UF1, BB_UF2, BB_UF3,           // unit ring: claimed unit written
+    BB_UE0, BB_UE1, BB_UE2, BB_UE3,           // unit ring: every reader has read it
+    BB_COUNT
 };
+
+constexpr int kBwdUnitRing = 4;       // claimed units buffered between the producer and the other roles
+constexpr int kBwdUnitReaders = 24;   // four MMA-issuing warps, 16 P/dS warps, 4 drain warps
+
+// Work counters of the persistent backward launches, one slot per launch in
+// flight: {next unit to claim, CTAs finished}.  The host gives each launch its
+// own slot (round robin); the launch's last CTA resets it to zero.
+constexpr int kBwdSchedSlots = 64;
+static __device__ unsigned int g_bwd_sched[kBwdSchedSlots][2];
 
 template <int D, bool PRECISE>
 struct BwdSmem {
@@ -134,9 +148,8 @@ struct BwdSmem {
     static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
     static constexpr int kdS = kdO + kStages * kQTile;      // dS^T (high part)  [kdSBufs]
     static constexpr int kdSlo = kdS + kdSBufs * kOp;       // precise: dS^T low part
-    static constexpr int kList = PRECISE ? kdSlo + kOp : kdSlo;
-    static constexpr int kListCap = 1024;                   // Q tiles staged from the plan
-    static constexpr int kStat = kList + kListCap * 4;      // -lse*log2e [kStages][64], D [kStages][64]
+    static constexpr int kUnit = PRECISE ? kdSlo + kOp : kdSlo;   // int [kBwdUnitRing][4]: unit ring
+    static constexpr int kStat = kUnit + kBwdUnitRing * 16;  // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
     static constexpr int kNumBar = BB_COUNT;
     static constexpr int kMisc = kBar + kNumBar * 8;
@@ -172,17 +185,14 @@ __global__ void __launch_bounds__(800, 1)
     uint8_t *sK = smem + S::kK, *sV = smem + S::kV;
     uint8_t *sQ = smem + S::kQ, *sdO = smem + S::kdO;
     uint8_t *sdS = smem + S::kdS, *sdSlo = smem + S::kdSlo;
-    int32_t *sList = reinterpret_cast<int32_t *>(smem + S::kList);
     constexpr int NST = S::kStages;
     float *sLse = reinterpret_cast<float *>(smem + S::kStat);     // [NST][64]
     float *sD = sLse + NST * 64;                                     // [NST][64]
+    volatile int *sUnit = reinterpret_cast<volatile int *>(smem + S::kUnit);   // [kBwdUnitRing][4]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
-    int *cnt_sh = reinterpret_cast<int *>(smem + S::kMisc + 8);
     int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
-
-    int *unit_sh = reinterpret_cast<int *>(smem + S::kMisc + 16);   // KV tile, head, batch
 
     const int warp = warp_id(), lane = lane_id();
     const PlanLayout &L = a.L;
@@ -190,23 +200,13 @@ __global__ void __launch_bounds__(800, 1)
 
     if (warp == 0) {
         const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(a.plan);
-        bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
-                  ph->bq == 128 && ph->bk == 128 && ph->q_row0 == L.q_row0 && ph->Nq == L.Nq;
-        // KV tiles longest column list first (the plan's bucketed order); ok is warp-uniform.
-        int ut = 0, uh = 0, ub = 0;
-        const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
-        if (ok)
-            ok = plan_unit(reinterpret_cast<const int32_t *>(a.plan + L.off_col_order),
-                           reinterpret_cast<const int32_t *>(a.plan + L.off_col_bstart), L.n_k, a.B, a.Hm, a.H, cta,
-                           &ut, &uh, &ub);
+        const bool ok = ph->magic == kPlanMagic && ph->B == L.B && ph->Hm == L.Hm && ph->N == L.N &&
+                        ph->bq == 128 && ph->bk == 128 && ph->q_row0 == L.q_row0 && ph->Nq == L.Nq;
         if (lane == 0) {
             if (!ok) set_status(a.status, FM_ERR_PLAN_MISMATCH);
             const bool aligned = (smem_u32(smem) & 1023u) == 0;   // 128-byte swizzle atoms need it
             if (!aligned) set_status(a.status, FM_ERR_UNSUPPORTED);
             *ok_sh = ok && aligned;
-            unit_sh[0] = ut; unit_sh[1] = uh; unit_sh[2] = ub;
-            const int us = ub * a.Hm + (a.Hm == 1 ? 0 : uh);
-            *cnt_sh = ok ? reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)us * L.n_k + ut] : 0;
             *abort = 0;
             mbar_init(&bars[BB_KV], 1);
             for (int s2 = 0; s2 < NST; ++s2) {
@@ -230,6 +230,12 @@ __global__ void __launch_bounds__(800, 1)
             mbar_init(&bars[BB_DQE0], 128);
             mbar_init(&bars[BB_DQE1], 128);
             mbar_init(&bars[BB_ACC], 1);
+            mbar_init(&bars[BB_KVE], 3);      // S^T, dP^T and dQ^T issuers, after a unit's last product
+            mbar_init(&bars[BB_ACCE], 512);   // P/dS threads, after the unit's dK, dV epilogue
+            for (int s2 = 0; s2 < kBwdUnitRing; ++s2) {
+                mbar_init(&bars[BB_UF0 + s2], 1);
+                mbar_init(&bars[BB_UE0 + s2], kBwdUnitReaders);
+            }
             mbar_init(&bars[BB_DRAIN0], 4);   // all four issuers
             mbar_init(&bars[BB_DRAIN1], 1);
             fence_barrier_init();
@@ -243,81 +249,157 @@ __global__ void __launch_bounds__(800, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const int kt = unit_sh[0], h = unit_sh[1], b = unit_sh[2];
-    const int sidx = b * a.Hm + (a.Hm == 1 ? 0 : h);
-    const int bh = b * a.H + h;
-    const int kb = kt * 128;
     // TMEM: dK, dV, then two score buffers b = half & 1: S^T at 256 + 128 b
     // (then P^T), dP^T at 320 + 128 b (then dQ^T, once dS^T has been written).
     const uint32_t tdK = tmem, tdV = tmem + 128, tS0 = tmem + 256, tdP0 = tmem + 320;
-    const int cnt = *cnt_sh;
-    const int32_t *glist =
-        reinterpret_cast<const int32_t *>(a.plan + L.off_col_list) + ((int64_t)sidx * L.n_k + kt) * L.n_q;
-    // Stage the list of non-skip Q tiles into shared memory (one global read
-    // per entry instead of one per entry per role).
-    for (int i = threadIdx.x; i < cnt && i < S::kListCap; i += blockDim.x) sList[i] = glist[i];
-    __syncthreads();
-    auto entry = [&](int t) { return t < S::kListCap ? sList[t] : glist[t]; };
-    // Flat iteration over 64-row halves of the listed Q tiles.  Only the last
-    // Q tile can have a second half beyond the Q rows, and it is last in the list.
     const int Nq = a.Nq;
-    const int n_it = (cnt > 0 && (entry(cnt - 1) & kTileMask) * 128 + 64 >= Nq) ? 2 * cnt - 1 : 2 * cnt;
-    auto q0_of = [&](int it) { return (entry(it >> 1) & kTileMask) * 128 + (it & 1) * 64; };
+
+    // Persistent CTAs with dynamic scheduling: the producer of each CTA claims
+    // the next work unit (b, h, 128-row KV tile) of the plan's longest-first
+    // order from the launch's counter whenever it is ready for one, so the CTAs
+    // that run at the same time work on neighbouring units of the order and the
+    // longest lists start first.  Claimed units pass to the other roles through
+    // a ring of kBwdUnitRing entries in shared memory (n_it = -1 ends it).
+    // Every role walks the same units and, across units, one CTA-wide sequence
+    // of 64-row Q halves G: stages, score and dS^T buffers and barrier phases
+    // follow G, so the next unit's loads and products start while the current
+    // unit's epilogue stores dK and dV.
+    const int64_t n_units = (int64_t)a.B * a.H * L.n_k;
+    unsigned int *sched = g_bwd_sched[a.sched_slot];
+    struct Unit {
+        int kt, bh, sidx, n_it;     // n_it: 64-row Q halves of the unit's list
+        const int32_t *list;
+    };
+    auto list_of = [&](const Unit &u) {
+        return reinterpret_cast<const int32_t *>(a.plan + L.off_col_list) + ((int64_t)u.sidx * L.n_k + u.kt) * L.n_q;
+    };
+    // First row of half it of a unit (only the last Q tile can have a second
+    // half beyond the Q rows, and it is last in the list).
+    auto q0_of = [&](const Unit &u, int it) { return (u.list[it >> 1] & kTileMask) * 128 + (it & 1) * 64; };
+    // Called by all 32 lanes of a warp; false on a plan that was not written by
+    // the classifier (reported).
+    auto unit_from = [&](int c, Unit &u) -> bool {
+        int ut = 0, uh = 0, ub = 0;
+        if (!plan_unit(reinterpret_cast<const int32_t *>(a.plan + L.off_col_order),
+                       reinterpret_cast<const int32_t *>(a.plan + L.off_col_bstart), L.n_k, a.B, a.Hm, a.H, c,
+                       &ut, &uh, &ub)) {
+            if (lane == 0) set_status(a.status, FM_ERR_PLAN_MISMATCH);
+            return false;
+        }
+        u.kt = ut;
+        u.bh = ub * a.H + uh;
+        u.sidx = ub * a.Hm + (a.Hm == 1 ? 0 : uh);
+        u.list = list_of(u);
+        const int cnt = reinterpret_cast<const int32_t *>(a.plan + L.off_col_cnt)[(int64_t)u.sidx * L.n_k + ut];
+        u.n_it = (cnt > 0 && (u.list[cnt - 1] & kTileMask) * 128 + 64 >= Nq) ? 2 * cnt - 1 : 2 * cnt;
+        return true;
+    };
+    // Unit k of the ring for a reading warp: waits until it has been claimed,
+    // reads it and releases the entry (lane 0 arrives for the warp); false when
+    // the sequence has ended or a wait gave up.
+    auto read_unit = [&](int k, Unit &u) -> bool {
+        const int slot = k % kBwdUnitRing;
+        if (!warp_wait(&bars[BB_UF0 + slot], (k / kBwdUnitRing) & 1, abort, a.status, a.wait_limit)) return false;
+        u.kt = sUnit[slot * 4 + 0];
+        u.bh = sUnit[slot * 4 + 1];
+        u.sidx = sUnit[slot * 4 + 2];
+        u.n_it = sUnit[slot * 4 + 3];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[BB_UE0 + slot]);
+        u.list = list_of(u);
+        return u.n_it >= 0;
+    };
 
     if (*ok_sh) {
         if (warp == 0) {
             // ------------------------------------------------ producer
-            if (lane == 0 && n_it > 0) {
+            // Claims units; per unit with halves: K, V (once the previous unit's
+            // S^T, dP^T and dQ^T have read them), then the Q and dO halves through
+            // the three-stage ring, lse and D staged with each.
+            if (lane == 0) {
                 tma_prefetch_desc(&tq); tma_prefetch_desc(&tk);
                 tma_prefetch_desc(&tv); tma_prefetch_desc(&tdo);
-                mbar_arrive_expect_tx(&bars[BB_KV], 2 * S::kKTile);
-#pragma unroll
-                for (int x = 0; x < NBOX; ++x) {
-                    tma_load_3d(sK + x * S::kKBox, &tk, &bars[BB_KV], x * 64, kb, bh);
-                    tma_load_3d(sV + x * S::kKBox, &tv, &bars[BB_KV], x * 64, kb, bh);
-                }
             }
-            int it = 0;
+            int G = 0;      // halves begun (CTA-wide)
+            int nkv = 0;    // K / V loads begun (units with halves)
             // Test hook: the first CTA withholds the Q/dO load of its second half,
             // so that the scores' wait for it runs out (never set by a product call).
-            const int withheld = (a.withhold && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) ? 1 : -1;
-            for (; it < n_it; ++it) {
-                const int q0 = q0_of(it);
-                const int st = it % NST;
-                // lse and D of the half's rows, loaded before the stage wait so
-                // the global latency overlaps it; rows beyond the Q rows get P = 0.
-                float lv[2], dv[2];
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int qi = q0 + lane + rr * 32;
-                    lv[rr] = INFINITY;
-                    dv[rr] = 0.f;
-                    if (qi < Nq) {
-                        lv[rr] = a.lse[(int64_t)bh * Nq + qi];
-                        dv[rr] = a.Dvec[(int64_t)bh * Nq + qi];
-                    }
+            const int withheld = (a.withhold && blockIdx.x == 0) ? 1 : -1;
+            bool run = true;
+            Unit u;
+            for (int k = 0; run; ++k) {
+                // Claim the next unit into ring entry k once every reader is done
+                // with the entry's previous unit.
+                const int slot = k % kBwdUnitRing;
+                if (k >= kBwdUnitRing &&
+                    !warp_wait(&bars[BB_UE0 + slot], ((k / kBwdUnitRing) - 1) & 1, abort, a.status, a.wait_limit))
+                    break;
+                int c = 0;
+                if (lane == 0) c = (int)atomicAdd(&sched[0], 1u);
+                c = __shfl_sync(0xffffffffu, c, 0);
+                bool valid = c < n_units;
+                if (valid && !unit_from(c, u)) valid = false;
+                if (lane == 0) {
+                    sUnit[slot * 4 + 0] = valid ? u.kt : 0;
+                    sUnit[slot * 4 + 1] = valid ? u.bh : 0;
+                    sUnit[slot * 4 + 2] = valid ? u.sidx : 0;
+                    sUnit[slot * 4 + 3] = valid ? u.n_it : -1;
+                    mbar_arrive(&bars[BB_UF0 + slot]);
                 }
-                if (it >= NST && !warp_wait(&bars[BB_QE0 + st], ((it / NST) - 1) & 1, abort, a.status, a.wait_limit)) break;
-                if (lane == 0 && it != withheld) {
-                    mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
+                if (!valid) break;
+                if (u.n_it == 0) continue;
+                if (nkv > 0 && !warp_wait(&bars[BB_KVE], (nkv - 1) & 1, abort, a.status, a.wait_limit)) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bars[BB_KV], 2 * S::kKTile);
 #pragma unroll
                     for (int x = 0; x < NBOX; ++x) {
-                        tma_load_3d(sQ + st * S::kQTile + x * S::kQBox, &tq, &bars[BB_QF0 + st], x * 64, q0, bh);
-                        tma_load_3d(sdO + st * S::kQTile + x * S::kQBox, &tdo, &bars[BB_QF0 + st], x * 64, q0, bh);
+                        tma_load_3d(sK + x * S::kKBox, &tk, &bars[BB_KV], x * 64, u.kt * 128, u.bh);
+                        tma_load_3d(sV + x * S::kKBox, &tv, &bars[BB_KV], x * 64, u.kt * 128, u.bh);
                     }
                 }
+                ++nkv;
+                for (int it = 0; it < u.n_it; ++it, ++G) {
+                    const int q0 = q0_of(u, it);
+                    const int st = G % NST;
+                    // lse and D of the half's rows, loaded before the stage wait so
+                    // the global latency overlaps it; rows beyond the Q rows get P = 0.
+                    float lv[2], dv[2];
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int r = lane + rr * 32;
-                    sLse[st * 64 + r] = (lv[rr] == -INFINITY) ? -INFINITY : -lv[rr] * 1.4426950408889634f;
-                    sD[st * 64 + r] = dv[rr];
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int qi = q0 + lane + rr * 32;
+                        lv[rr] = INFINITY;
+                        dv[rr] = 0.f;
+                        if (qi < Nq) {
+                            lv[rr] = a.lse[(int64_t)u.bh * Nq + qi];
+                            dv[rr] = a.Dvec[(int64_t)u.bh * Nq + qi];
+                        }
+                    }
+                    if (G >= NST &&
+                        !warp_wait(&bars[BB_QE0 + st], ((G / NST) - 1) & 1, abort, a.status, a.wait_limit)) {
+                        run = false;
+                        break;
+                    }
+                    if (lane == 0 && G != withheld) {
+                        mbar_arrive_expect_tx(&bars[BB_QF0 + st], 2 * S::kQTile);
+#pragma unroll
+                        for (int x = 0; x < NBOX; ++x) {
+                            tma_load_3d(sQ + st * S::kQTile + x * S::kQBox, &tq, &bars[BB_QF0 + st], x * 64, q0, u.bh);
+                            tma_load_3d(sdO + st * S::kQTile + x * S::kQBox, &tdo, &bars[BB_QF0 + st], x * 64, q0, u.bh);
+                        }
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int r = lane + rr * 32;
+                        sLse[st * 64 + r] = (lv[rr] == -INFINITY) ? -INFINITY : -lv[rr] * 1.4426950408889634f;
+                        sD[st * 64 + r] = dv[rr];
+                    }
+                    mbar_arrive(&bars[BB_QF0 + st]);     // 32 arrivals after the stores (+1 expect_tx)
                 }
-                mbar_arrive(&bars[BB_QF0 + st]);     // 32 arrivals after the stores (+1 expect_tx)
             }
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
-                if (n_it > 0) mbar_wait_drain(&bars[BB_KV], 0, a.status, a.wait_limit);
-                for (int k2 = (it > NST ? it - NST : 0); k2 < it; ++k2)
+                if (nkv > 0) mbar_wait_drain(&bars[BB_KV], (nkv - 1) & 1, a.status, a.wait_limit);
+                for (int k2 = (G > NST ? G - NST : 0); k2 < G; ++k2)
                     if (k2 != withheld) mbar_wait_drain(&bars[BB_QF0 + (k2 % NST)], (k2 / NST) & 1, a.status, a.wait_limit);
             }
         } else if (warp == 1 || warp >= 22) {
@@ -328,84 +410,112 @@ __global__ void __launch_bounds__(800, 1)
             // dQ^T (once dS^T is written), warp 24 dV then dK (once P^T, dS^T are
             // written).  A Q/dO stage is released by the S^T, dP^T and dV/dK
             // threads, a dS^T buffer by the dQ^T and dK products.
+            // Per unit the S^T, dP^T and dQ^T threads wait for the unit's K and V
+            // (and commit the K / V release after their last product); the dV/dK
+            // thread, which reads neither, instead waits until the previous unit's
+            // epilogue has read dK and dV before its first product overwrites them.
+            // All lanes walk the units (the ring is read warp-wide); lane 0 issues.
             const int role = (warp == 1) ? 0 : (warp == 23) ? 1 : (warp == 22) ? 2 : 3;
-            if (lane == 0 && n_it > 0) {
-                constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
-                constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
-                constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
-                constexpr int NPART = PRECISE ? 2 : 1;
-                const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024);      // K, K-major
-                const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);      // V, K-major
-                const uint64_t dKm = sdesc_sw128(smem_u32(sK), S::kKBox, 1024); // K, MN-major
-                const uint64_t dSk[2] = {sdesc_sw128(smem_u32(sdS), 16, 1024), sdesc_sw128(smem_u32(sdSlo), 16, 1024)};
-                const uint64_t dSm[2] = {sdesc_sw128(smem_u32(sdS), S::kKBox, 1024),
-                                         sdesc_sw128(smem_u32(sdSlo), S::kKBox, 1024)};
-                bool ok = mbar_wait(&bars[BB_KV], 0, abort, a.status, a.wait_limit);
-                for (int it = 0; ok && it < n_it; ++it) {
-                    const int st = it % NST;
-                    if (role <= 1) {
-                        const int b = it & 1;
-                        // The S^T columns of buffer b are free once dV has read the P^T
-                        // of the half that used them before, the dP^T columns once the
-                        // drain holds that half's dQ^T (both imply the scores were read).
-                        uint64_t *free_bar = &bars[(role == 0 ? BB_PE0 : BB_DQE0) + b];
-                        if (!mbar_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status, a.wait_limit) ||
-                            (it >= 2 && !mbar_wait(free_bar, ((it >> 1) - 1) & 1, abort, a.status, a.wait_limit))) { ok = false; break; }
-                        tc_fence_after();
-                        const uint64_t dA = role == 0 ? dKk : dVk;                    // K for S^T, V for dP^T
-                        const uint64_t dB = sdesc_sw128(smem_u32((role == 0 ? sQ : sdO) + st * S::kQTile), 16, 1024);
-                        const uint32_t tD = (role == 0 ? tS0 : tdP0) + b * 128;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
-                            const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
-                            mma_ss(tD, sdesc_add(dA, ok_), sdesc_add(dB, oq), idS, kk > 0);
-                        }
-                        tc_commit(&bars[(role == 0 ? BB_SF0 : BB_SFD0) + b]);
-                        tc_commit(&bars[BB_QE0 + st]);
-                    } else {
-                        const int qb = it & 1;         // score buffer: P^T in its S^T columns, dQ^T in its dP^T columns
-                        const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;   // dS^T buffer of this half
-                        const uint32_t pbo = pb * S::kOp;
-                        if (role == 2) {
-                            if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
+            constexpr uint32_t idS = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t idKV = idesc_bf16(128, D, false, true);
+            constexpr uint32_t idQ = idesc_bf16(128, 64, true, true);
+            constexpr int NPART = PRECISE ? 2 : 1;
+            const uint64_t dKk = sdesc_sw128(smem_u32(sK), 16, 1024);      // K, K-major
+            const uint64_t dVk = sdesc_sw128(smem_u32(sV), 16, 1024);      // V, K-major
+            const uint64_t dKm = sdesc_sw128(smem_u32(sK), S::kKBox, 1024); // K, MN-major
+            const uint64_t dSk[2] = {sdesc_sw128(smem_u32(sdS), 16, 1024), sdesc_sw128(smem_u32(sdSlo), 16, 1024)};
+            const uint64_t dSm[2] = {sdesc_sw128(smem_u32(sdS), S::kKBox, 1024),
+                                     sdesc_sw128(smem_u32(sdSlo), S::kKBox, 1024)};
+            int G = 0;      // halves begun (CTA-wide)
+            int nu = 0;     // units with halves begun
+            bool run = true;
+            Unit u;
+            for (int k = 0; run; ++k) {
+                if (!read_unit(k, u)) break;
+                if (u.n_it == 0) continue;
+                if (lane == 0) {
+                    if (role != 3) run = mbar_wait(&bars[BB_KV], nu & 1, abort, a.status, a.wait_limit);
+                    else if (nu > 0) run = mbar_wait(&bars[BB_ACCE], (nu - 1) & 1, abort, a.status, a.wait_limit);
+                    for (int it = 0; run && it < u.n_it; ++it, ++G) {
+                        const int st = G % NST;
+                        if (role <= 1) {
+                            const int b = G & 1;
+                            // The S^T columns of buffer b are free once dV has read the P^T
+                            // of the half that used them before, the dP^T columns once the
+                            // drain holds that half's dQ^T (both imply the scores were read).
+                            uint64_t *free_bar = &bars[(role == 0 ? BB_PE0 : BB_DQE0) + b];
+                            if (!mbar_wait(&bars[BB_QF0 + st], (G / NST) & 1, abort, a.status, a.wait_limit) ||
+                                (G >= 2 && !mbar_wait(free_bar, ((G >> 1) - 1) & 1, abort, a.status, a.wait_limit))) {
+                                run = false;
+                                break;
+                            }
                             tc_fence_after();
+                            const uint64_t dA = role == 0 ? dKk : dVk;                    // K for S^T, V for dP^T
+                            const uint64_t dB = sdesc_sw128(smem_u32((role == 0 ? sQ : sdO) + st * S::kQTile), 16, 1024);
+                            const uint32_t tD = (role == 0 ? tS0 : tdP0) + b * 128;
 #pragma unroll
-                            for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_ss(tdP0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048),
-                                           idQ, (part > 0 || kk > 0));
-                            tc_commit(&bars[BB_DQF0 + qb]);
-                            tc_commit(&bars[BB_DSE0 + pb]);
-                        } else {
-                            const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
-                            const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
-                            if (!mbar_wait(&bars[BB_PF0 + qb], (it >> 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
-                            tc_fence_after();
-                            // P^T of the 16 columns kk: TMEM columns [16 kk, 16 kk + 8) of
-                            // the S^T block (the low terms in the next 8 columns).
-#pragma unroll
-                            for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    mma_ts(tdV, tS0 + qb * 128 + kk * 16 + part * 8, sdesc_add(dOm, kk * 2048), idKV,
-                                           (it > 0 || part > 0 || kk > 0));
-                            tc_commit(&bars[BB_PE0 + qb]);
-                            if (!mbar_wait(&bars[BB_DF0 + qb], (it >> 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
-                            tc_fence_after();
-#pragma unroll
-                            for (int part = 0; part < NPART; ++part)
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk)
-                                    mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
-                                           (it > 0 || part > 0 || kk > 0));
-                            tc_commit(&bars[BB_DSE0 + pb]);
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t ok_ = (kk >> 2) * S::kKBox + (kk & 3) * 32;
+                                const uint32_t oq = (kk >> 2) * S::kQBox + (kk & 3) * 32;
+                                mma_ss(tD, sdesc_add(dA, ok_), sdesc_add(dB, oq), idS, kk > 0);
+                            }
+                            tc_commit(&bars[(role == 0 ? BB_SF0 : BB_SFD0) + b]);
                             tc_commit(&bars[BB_QE0 + st]);
+                        } else {
+                            const int qb = G & 1;          // score buffer: P^T in its S^T columns, dQ^T in its dP^T columns
+                            const int pb = (S::kdSBufs == 2) ? (G & 1) : 0;   // dS^T buffer of this half
+                            const uint32_t pbo = pb * S::kOp;
+                            if (role == 2) {
+                                if (!mbar_wait(&bars[BB_DF0 + qb], (G >> 1) & 1, abort, a.status, a.wait_limit)) {
+                                    run = false;
+                                    break;
+                                }
+                                tc_fence_after();
+#pragma unroll
+                                for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                                    for (int kk = 0; kk < 8; ++kk)
+                                        mma_ss(tdP0 + qb * 128, sdesc_add(dKm, kk * 2048), sdesc_add(dSm[part], pbo + kk * 2048),
+                                               idQ, (part > 0 || kk > 0));
+                                tc_commit(&bars[BB_DQF0 + qb]);
+                                tc_commit(&bars[BB_DSE0 + pb]);
+                            } else {
+                                const uint64_t dQm = sdesc_sw128(smem_u32(sQ + st * S::kQTile), S::kQBox, 1024);
+                                const uint64_t dOm = sdesc_sw128(smem_u32(sdO + st * S::kQTile), S::kQBox, 1024);
+                                if (!mbar_wait(&bars[BB_PF0 + qb], (G >> 1) & 1, abort, a.status, a.wait_limit)) {
+                                    run = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                // P^T of the 16 columns kk: TMEM columns [16 kk, 16 kk + 8) of
+                                // the S^T block (the low terms in the next 8 columns).
+#pragma unroll
+                                for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        mma_ts(tdV, tS0 + qb * 128 + kk * 16 + part * 8, sdesc_add(dOm, kk * 2048), idKV,
+                                               (it > 0 || part > 0 || kk > 0));
+                                tc_commit(&bars[BB_PE0 + qb]);
+                                if (!mbar_wait(&bars[BB_DF0 + qb], (G >> 1) & 1, abort, a.status, a.wait_limit)) {
+                                    run = false;
+                                    break;
+                                }
+                                tc_fence_after();
+#pragma unroll
+                                for (int part = 0; part < NPART; ++part)
+#pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        mma_ss(tdK, sdesc_add(dSk[part], pbo + kk * 32), sdesc_add(dQm, kk * 2048), idKV,
+                                               (it > 0 || part > 0 || kk > 0));
+                                tc_commit(&bars[BB_DSE0 + pb]);
+                                tc_commit(&bars[BB_QE0 + st]);
+                            }
                         }
                     }
+                    if (run) tc_commit(&bars[role == 3 ? BB_ACC : BB_KVE]);
                 }
-                if (ok && role == 3) tc_commit(&bars[BB_ACC]);
+                ++nu;
+                run = __shfl_sync(0xffffffffu, run, 0);
             }
             if (lane == 0) {
                 tc_commit(&bars[BB_DRAIN0]);
@@ -420,24 +530,31 @@ __global__ void __launch_bounds__(800, 1)
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;       // KV row within the tile
             const int c0 = wg * CW;                  // first column of this warpgroup
-            const int j = kb + r;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            int G = 0;      // halves begun (CTA-wide)
+            int nu = 0;     // units with halves finished
+            bool ok = true;
+            Unit u;
+            for (int k = 0; ok; ++k) {
+            if (!read_unit(k, u)) break;
+            const int kb = u.kt * 128;
+            const int j = kb + r;
             int lo0 = 0, lolen = 0, up0 = 0, uplen = 0x7fffffff;   // beyond N: masked everywhere
             if (j < N) {
-                const int64_t o = (int64_t)sidx * N + j;
+                const int64_t o = (int64_t)u.sidx * N + j;
                 const int l0 = a.lts[o], l1 = a.lte[o], u0 = a.uts[o], u1 = a.ute[o];
                 lo0 = l0; lolen = max(l1 - l0, 0); up0 = u0; uplen = max(u1 - u0, 0);
             }
             const bool kv_tail = kb + 128 > N;
-            bool ok = true;
-            for (int it = 0; it < n_it; ++it) {
-                const int q0 = q0_of(it);
-                const bool pred = ((entry(it >> 1) >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
-                const int st = it % NST;
-                const int b = it & 1;                     // score buffer
+            for (int it = 0; it < u.n_it; ++it, ++G) {
+                const int e = u.list[it >> 1];
+                const int q0 = (e & kTileMask) * 128 + (it & 1) * 64;
+                const bool pred = ((e >> kLabelShift) == FM_TILE_PARTIAL) || kv_tail;
+                const int st = G % NST;
+                const int b = G & 1;                      // score buffer
                 // P needs only S^T: dP^T is waited for after P^T has been handed to dV.
-                if (!warp_wait(&bars[BB_SF0 + b], (it >> 1) & 1, abort, a.status, a.wait_limit) ||
-                    !warp_wait(&bars[BB_QF0 + st], (it / NST) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
+                if (!warp_wait(&bars[BB_SF0 + b], (G >> 1) & 1, abort, a.status, a.wait_limit) ||
+                    !warp_wait(&bars[BB_QF0 + st], (G / NST) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
                 tc_fence_after();
                 uint32_t sraw[CW], draw[CW];
                 tmem_ld16(tS0 + b * 128 + lane_off + c0, sraw);
@@ -489,7 +606,7 @@ __global__ void __launch_bounds__(800, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bars[BB_PF0 + b]);
-                if (!warp_wait(&bars[BB_SFD0 + b], (it >> 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
+                if (!warp_wait(&bars[BB_SFD0 + b], (G >> 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
                 tc_fence_after();
                 tmem_ld16(tdP0 + b * 128 + lane_off + c0, draw);
                 tmem_ld_wait();
@@ -501,9 +618,9 @@ __global__ void __launch_bounds__(800, 1)
                 }
                 // dS^T (its buffer is free once dK, dQ^T of the half that last
                 // used it have completed, normally long ago), announced on DF.
-                const int pb = (S::kdSBufs == 2) ? (it & 1) : 0;
+                const int pb = (S::kdSBufs == 2) ? (G & 1) : 0;
                 const int back = S::kdSBufs;                 // halves between two uses of a dS^T buffer
-                if (it >= back && !warp_wait(&bars[BB_DSE0 + pb], ((it / back) - 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
+                if (G >= back && !warp_wait(&bars[BB_DSE0 + pb], ((G / back) - 1) & 1, abort, a.status, a.wait_limit)) { ok = false; break; }
                 uint8_t *bdS = sdS + pb * S::kOp;
                 // Row r of a 128-byte-swizzled tile: 16-byte chunk c lives at c ^ (r & 7).
 #pragma unroll
@@ -525,45 +642,53 @@ __global__ void __launch_bounds__(800, 1)
                 mbar_arrive(&bars[BB_DF0 + b]);
             }
             // ------------------------------------------------ dK, dV epilogue
-            // Warpgroups 0, 1 store the two column halves of dK; 2, 3 of dV.
-            if (ok && (n_it == 0 || warp_wait(&bars[BB_ACC], 0, abort, a.status, a.wait_limit))) {
-                tc_fence_after();
-                const bool row_in = j < N;
-                const int64_t row = (int64_t)bh * N + j;
-                const bool is_dk = wg < 2;
-                const uint32_t tsrc = is_dk ? tdK : tdV;
-                const float mul = is_dk ? a.scale : 1.f;
-                void *dst = is_dk ? a.dk : a.dv;
-                const int cbase = (wg & 1) * (D / 2);
+            // Warpgroups 0, 1 store the two column halves of dK; 2, 3 of dV.  The
+            // accumulators are released to the next unit's first dV / dK product
+            // once read; a unit without halves stores zeros.
+            if (!ok) break;
+            if (u.n_it > 0 && !warp_wait(&bars[BB_ACC], nu & 1, abort, a.status, a.wait_limit)) break;
+            tc_fence_after();
+            const bool row_in = j < N;
+            const int64_t row = (int64_t)u.bh * N + j;
+            const bool is_dk = wg < 2;
+            const uint32_t tsrc = is_dk ? tdK : tdV;
+            const float mul = is_dk ? a.scale : 1.f;
+            void *dst = is_dk ? a.dk : a.dv;
+            const int cbase = (wg & 1) * (D / 2);
 #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    const int col = cbase + cc * 32;
-                    uint32_t v[32];
-                    if (n_it > 0) {            // warp-uniform: every lane loads
-                        tmem_ld32(tsrc + lane_off + col, v);
-                        tmem_ld_wait();
-                        tmem_reg_fence(v);
-                    } else {
+            for (int cc = 0; cc < D / 64; ++cc) {
+                const int col = cbase + cc * 32;
+                uint32_t v[32];
+                if (u.n_it > 0) {          // warp-uniform: every lane loads
+                    tmem_ld32(tsrc + lane_off + col, v);
+                    tmem_ld_wait();
+                    tmem_reg_fence(v);
+                } else {
 #pragma unroll
-                        for (int u = 0; u < 32; ++u) v[u] = 0u;
-                    }
-                    if (!row_in) continue;
-                    if (a.g_f32) {
-                        float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + col);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u)
-                            pp[u] = make_float4(__uint_as_float(v[4 * u]) * mul, __uint_as_float(v[4 * u + 1]) * mul,
-                                                __uint_as_float(v[4 * u + 2]) * mul, __uint_as_float(v[4 * u + 3]) * mul);
-                    } else {
-                        uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + col);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            pp[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u]) * mul, __uint_as_float(v[8 * u + 1]) * mul),
-                                               pack_bf16x2(__uint_as_float(v[8 * u + 2]) * mul, __uint_as_float(v[8 * u + 3]) * mul),
-                                               pack_bf16x2(__uint_as_float(v[8 * u + 4]) * mul, __uint_as_float(v[8 * u + 5]) * mul),
-                                               pack_bf16x2(__uint_as_float(v[8 * u + 6]) * mul, __uint_as_float(v[8 * u + 7]) * mul));
-                    }
+                    for (int q = 0; q < 32; ++q) v[q] = 0u;
                 }
+                if (!row_in) continue;
+                if (a.g_f32) {
+                    float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + col);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        pp[q] = make_float4(__uint_as_float(v[4 * q]) * mul, __uint_as_float(v[4 * q + 1]) * mul,
+                                            __uint_as_float(v[4 * q + 2]) * mul, __uint_as_float(v[4 * q + 3]) * mul);
+                } else {
+                    uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + col);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        pp[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                                           pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                                           pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                                           pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                }
+            }
+            if (u.n_it > 0) {
+                tc_fence_before();
+                mbar_arrive(&bars[BB_ACCE]);
+                ++nu;
+            }
             }
         } else if (warp < 22) {
             // ------------------------------------------------ dQ drain
@@ -580,10 +705,17 @@ __global__ void __launch_bounds__(800, 1)
             // In a register: the reductions' memory clobbers would otherwise make the
             // compiler reload the parameter for every element.
             const float dq_mul = a.dq_mul;
-            for (int it = 0; it < n_it; ++it) {
-                const int q0 = q0_of(it);
-                const int qb = it & 1;
-                if (!warp_wait(&bars[BB_DQF0 + qb], (it >> 1) & 1, abort, a.status, a.wait_limit)) break;
+            int G = 0;      // halves begun (CTA-wide)
+            bool run = true;
+            Unit u;
+            for (int k = 0; run && read_unit(k, u); ++k)
+            for (int it = 0; it < u.n_it; ++it, ++G) {
+                const int q0 = q0_of(u, it);
+                const int qb = G & 1;
+                if (!warp_wait(&bars[BB_DQF0 + qb], (G >> 1) & 1, abort, a.status, a.wait_limit)) {
+                    run = false;
+                    break;
+                }
                 tc_fence_after();
                 uint32_t v[2][32];
                 tmem_ld32(tdP0 + qb * 128 + lane_off, v[0]);
@@ -607,7 +739,7 @@ __global__ void __launch_bounds__(800, 1)
                 tc_fence_before();
                 mbar_arrive(&bars[BB_DQE0 + qb]);   // score buffer qb is free again
                 if (!has_cols) continue;
-                float *dst = a.dq_acc + ((int64_t)bh * Nq + q0) * D + dd;
+                float *dst = a.dq_acc + ((int64_t)u.bh * Nq + q0) * D + dd;
                 const int lim = min(64, Nq - q0);      // rows beyond the Q rows: nothing to add
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
@@ -620,6 +752,16 @@ __global__ void __launch_bounds__(800, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    // The launch's last CTA returns the work counters to zero for the next
+    // launch that gets this slot (every claim precedes its CTA's count here).
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&sched[1], 1u) == gridDim.x - 1) {
+            sched[0] = 0;
+            sched[1] = 0;
+            __threadfence();
+        }
     }
 }
 
@@ -667,13 +809,23 @@ static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
 {
     constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
     if (!bwd_smem_ready<D, PRECISE>()) return FM_ERR_CUDA;
+    // Persistent: one CTA per SM (shared memory and 512 TMEM columns allow no
+    // second one), each claiming units of the plan's order.
+    const int64_t units = (int64_t)a.B * a.H * a.L.n_k;
+    const int sms = device_sm_count();
+    if (sms <= 0) return FM_ERR_CUDA;
+    const unsigned grid = (unsigned)(units < sms ? units : sms);
+    static std::atomic<unsigned> next_slot{0};
+    BwdArgs args = a;
+    args.sched_slot = (int)(next_slot.fetch_add(1, std::memory_order_relaxed) % kBwdSchedSlots);
     ProfScope ps(kKBwd, stream);
-    fm_bwd_kernel<D, PRECISE><<<dim3(a.L.n_k, a.H, a.B), 800, smem, stream>>>(tq, tk, tv, tdo, a);
+    fm_bwd_kernel<D, PRECISE><<<grid, 800, smem, stream>>>(tq, tk, tv, tdo, args);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
 fm_status fm_bwd_prepare(int d, bool precise)
 {
+    if (device_sm_count() <= 0) return FM_ERR_CUDA;   // cached before any stream capture
     const bool ok = d == 128 ? (precise ? bwd_smem_ready<128, true>() : bwd_smem_ready<128, false>())
                              : (precise ? bwd_smem_ready<64, true>() : bwd_smem_ready<64, false>());
     return ok ? FM_OK : FM_ERR_CUDA;

@@ -168,6 +168,7 @@ struct BwdArgs {
     int g_f32;
     long long wait_limit; // bound of every device-side wait, SM cycles (kWaitLimitCycles)
     int withhold;         // test hook (0 in every product launch): CTA 0 skips its second Q/dO load
+    int sched_slot;       // work-counter slot of this launch (persistent scheduling)
 };
 
 // Kernel ids for the profiler.
