@@ -47,8 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel, the hash of the source it was taken on (stale entries are ignored)
 # and the workload.
 NCU_TRAFFIC = {
-    ("bwd", "e51d130dcc45d28f", "long_packing_128k"): 4311.90e6 + 2896.70e6,
-    ("bwd", "e51d130dcc45d28f", "sliding_window"): 831.45e6 + 762.06e6,
+    ("bwd", "2fdf3f2511528954", "long_packing_128k"): 4307.085e6 + 2893.266e6,
 }
 
 
