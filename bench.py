@@ -10,7 +10,8 @@ in HBM.  `e2e` repeats the step through the C ABI from pinned host buffers:
 row-form mask conversion on the host, host-to-device copies of Q, K, V, dO
 and the bounds, the device work, and device-to-host copies of O, lse, dQ,
 dK, dV, all inside the timed region; the copies run on their own streams
-with two buffer sets, so one step's copies overlap its neighbours' compute.  `graph` times the same step captured
+with two buffer sets, so one step's copies overlap its neighbours' compute.  `e2e_bf16_outputs` repeats it with bf16
+O, dQ, dK, dV (half the bytes read back).  `graph` times the same step captured
 once into a CUDA graph (fm_step_graph_create) and replayed, one launch per
 step.  `fp8_fwd` times the forward on e4m3 inputs (fm_attn_fwd_fp8) and the
 quantization of Q, K, V beside it.
@@ -47,7 +48,6 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel, the hash of the source it was taken on (stale entries are ignored)
 # and the workload.
 NCU_TRAFFIC = {
-    ("bwd", "2fdf3f2511528954", "long_packing_128k"): 4307.085e6 + 2893.266e6,
 }
 
 
@@ -60,10 +60,12 @@ def load_peaks():
 
 
 def src_hash(name):
-    path = os.path.join(ROOT, "long_context_fm_gb300", "csrc", name)
+    """Hash of a kernel's source, its PTX helpers and the classifier (whose
+    work order decides which tiles run together, hence the DRAM traffic)."""
+    csrc = os.path.join(ROOT, "long_context_fm_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (path, os.path.join(ROOT, "long_context_fm_gb300", "csrc", "fm_ptx.cuh")):
-        h.update(open(f, "rb").read())
+    for f in (name, "fm_ptx.cuh", "fm_classify.cu"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -317,82 +319,89 @@ def run_fm(args, rank, world, local_rank):
     rows = m["rows"]
     multi = m["row_intervals"]
 
-    def device_set(first):
-        if first:
-            return dict(q=q, k=k, v=v, dO=dO, o=o, lse=lse, dq=dq, dk=dk, dv=dv, bnd=bnd, bounds=bounds)
-        st = dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v), dO=torch.empty_like(dO),
-                  o=torch.empty_like(o), lse=torch.empty_like(lse), dq=torch.empty_like(dq),
-                  dk=torch.empty_like(dk), dv=torch.empty_like(dv), bnd=[torch.empty_like(b) for b in bnd])
-        st["bounds"] = fm.make_bounds(*st["bnd"])
-        return st
+    def run_e2e(out_dtype):
+        """Pipelined end-to-end steps with O, dQ, dK, dV of out_dtype (lse fp32);
+        returns seconds per step and the bytes copied in and out per step."""
+        def device_set():
+            st = dict(q=torch.empty_like(q), k=torch.empty_like(k), v=torch.empty_like(v), dO=torch.empty_like(dO),
+                      lse=torch.empty_like(lse), bnd=[torch.empty_like(b_) for b_ in bnd])
+            for key in ("o", "dq", "dk", "dv"):
+                st[key] = torch.empty(q.shape, dtype=out_dtype, device=dev)
+            st["bounds"] = fm.make_bounds(*st["bnd"])
+            return st
 
-    sets = [device_set(True), device_set(False)]
-    host_out = [dict((key, torch.empty_like(sets[0][key], device="cpu").pin_memory())
-                     for key in ("o", "lse", "dq", "dk", "dv")) for _ in range(2)]
-    host_bnd = [[torch.empty(bnd[0].shape, dtype=torch.int32).pin_memory() for _ in range(4)] for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * bnd[0].numel() * 4
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
-    s_h2d, s_cmp, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_h2d = [torch.cuda.Event() for _ in range(2)]
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]
-    ev_d2h = [torch.cuda.Event() for _ in range(2)]
+        sets = [device_set(), device_set()]
+        host_out = [dict((key, torch.empty_like(sets[0][key], device="cpu").pin_memory())
+                         for key in ("o", "lse", "dq", "dk", "dv")) for _ in range(2)]
+        host_bnd = [[torch.empty(bnd[0].shape, dtype=torch.int32).pin_memory() for _ in range(4)] for _ in range(2)]
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + 4 * bnd[0].numel() * 4
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+        s_h2d, s_cmp, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_h2d = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
+        ev_d2h = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_issue(i):
-        sidx = i % 2
-        bs, hb = sets[sidx], host_bnd[sidx]
-        if rows is not None:                                     # host conversion of the row form
-            cols = fm.fm_mask_from_rows(*rows)
-        elif multi is not None:                                  # several intervals per row
-            cols = fm.fm_mask_from_row_intervals(*multi)
-        else:
-            cols = [m[x] for x in ("lts", "lte", "uts", "ute")]
-        if i >= 2:
-            ev_h2d[sidx].synchronize()                           # hb is still being copied from
-        for dst, src in zip(hb, cols):
-            dst.numpy()[...] = src
-        with torch.cuda.stream(s_h2d):
+        def e2e_issue(i):
+            sidx = i % 2
+            bs, hb = sets[sidx], host_bnd[sidx]
+            if rows is not None:                                     # host conversion of the row form
+                cols = fm.fm_mask_from_rows(*rows)
+            elif multi is not None:                                  # several intervals per row
+                cols = fm.fm_mask_from_row_intervals(*multi)
+            else:
+                cols = [m[x] for x in ("lts", "lte", "uts", "ute")]
             if i >= 2:
-                s_h2d.wait_event(ev_cmp[sidx])                   # the set's inputs are free again
-            for dst, src in zip(bs["bnd"], hb):
-                dst.copy_(src, non_blocking=True)
-            for key, src in zip(("q", "k", "v", "dO"), (hq, hk, hv, hdo)):
-                bs[key].copy_(src, non_blocking=True)
-            ev_h2d[sidx].record(s_h2d)
-        with torch.cuda.stream(s_cmp):
-            s_cmp.wait_event(ev_h2d[sidx])
-            if i >= 2:
-                s_cmp.wait_event(ev_d2h[sidx])                   # the set's outputs have been read out
-            fm.fm_tile_classify(bs["bounds"], plan, status, stream=s_cmp)
-            fm.fm_attn_fwd(bs["q"], bs["k"], bs["v"], bs["bounds"], plan, scale, bs["o"], bs["lse"], status,
-                           stream=s_cmp, flags=flags)
-            fm.fm_attn_bwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["lse"], bs["dO"], bs["bounds"], plan, scale,
-                           bs["dq"], bs["dk"], bs["dv"], ws, status, stream=s_cmp, flags=flags)
-            ev_cmp[sidx].record(s_cmp)
-        with torch.cuda.stream(s_d2h):
-            s_d2h.wait_event(ev_cmp[sidx])
-            for key, dst in host_out[sidx].items():
-                dst.copy_(bs[key], non_blocking=True)
-            ev_d2h[sidx].record(s_d2h)
+                ev_h2d[sidx].synchronize()                           # hb is still being copied from
+            for dst, src in zip(hb, cols):
+                dst.numpy()[...] = src
+            with torch.cuda.stream(s_h2d):
+                if i >= 2:
+                    s_h2d.wait_event(ev_cmp[sidx])                   # the set's inputs are free again
+                for dst, src in zip(bs["bnd"], hb):
+                    dst.copy_(src, non_blocking=True)
+                for key, src in zip(("q", "k", "v", "dO"), (hq, hk, hv, hdo)):
+                    bs[key].copy_(src, non_blocking=True)
+                ev_h2d[sidx].record(s_h2d)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_h2d[sidx])
+                if i >= 2:
+                    s_cmp.wait_event(ev_d2h[sidx])                   # the set's outputs have been read out
+                fm.fm_tile_classify(bs["bounds"], plan, status, stream=s_cmp)
+                fm.fm_attn_fwd(bs["q"], bs["k"], bs["v"], bs["bounds"], plan, scale, bs["o"], bs["lse"], status,
+                               stream=s_cmp, flags=flags)
+                fm.fm_attn_bwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["lse"], bs["dO"], bs["bounds"], plan, scale,
+                               bs["dq"], bs["dk"], bs["dv"], ws, status, stream=s_cmp, flags=flags)
+                ev_cmp[sidx].record(s_cmp)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_cmp[sidx])
+                for key, dst in host_out[sidx].items():
+                    dst.copy_(bs[key], non_blocking=True)
+                ev_d2h[sidx].record(s_d2h)
 
-    torch.cuda.synchronize(dev)
-    for i in range(2):
-        e2e_issue(i)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_steps = max(2, min(args.steps, 8))
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        e2e_issue(i + 2)
-    torch.cuda.synchronize(dev)
-    barrier()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {int(status.item())} in the end-to-end steps")
+        torch.cuda.synchronize(dev)
+        for i in range(2):
+            e2e_issue(i)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_steps = max(2, min(args.steps, 8))
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            e2e_issue(i + 2)
+        torch.cuda.synchronize(dev)
+        barrier()
+        sec = (time.perf_counter() - t0) / e2e_steps
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in the end-to-end steps")
+        del sets
+        return sec, h2d, d2h
 
-    ms_step, e2e_s, graph_ms = max_over_ranks([ms_step, e2e_s, graph_ms], world, dev)
+    e2e_s, h2d, d2h = run_e2e(torch.float32)
+    e2e16_s, _, d2h16 = run_e2e(torch.bfloat16)
+
+    ms_step, e2e_s, e2e16_s, graph_ms = max_over_ranks([ms_step, e2e_s, e2e16_s, graph_ms], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
                 avg=avg, launches=launches, clocks=clocks.summary(), e2e_s=e2e_s, h2d=h2d, d2h=d2h,
-                graph_ms=graph_ms, fp8=fp8, flags=flags, nnz_tiles=nnz_tiles)
+                e2e16_s=e2e16_s, d2h16=d2h16, graph_ms=graph_ms, fp8=fp8, flags=flags, nnz_tiles=nnz_tiles)
 
 
 def mask_description(wl):
@@ -552,6 +561,9 @@ def main():
             "clocks": r["clocks"],
             "e2e": {"value": world * step_flops / r["e2e_s"] / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+            "e2e_bf16_outputs": {"value": world * step_flops / r["e2e16_s"] / 1e12, "unit": "TFLOP/s",
+                                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h16"],
+                                 "note": "the same end-to-end step with bf16 O, dQ, dK, dV (lse fp32)"},
         }
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = {k_: v_ for k_, v_ in cpu_baseline_sample(wl, W.make_mask(wl), max_docs=7).items()

@@ -82,15 +82,30 @@ def test_bucket_rule_is_monotone():
     assert np.all(np.diff(b[1:]) <= 0)
 
 
+def _group_weights(lab):
+    """Per KV tile of one (b, hm) segment (rows of `lab` = KV tiles, columns =
+    Q tiles): the longest non-skip list among the KV tiles whose lists end at
+    the same Q tile; 0 for an empty list."""
+    nz = lab != oracle.SKIP
+    cnt = nz.sum(axis=1)
+    key = np.where(cnt > 0, nz.shape[1] - 1 - np.argmax(nz[:, ::-1], axis=1), -1)
+    w = np.zeros_like(cnt)
+    for k in np.unique(key[key >= 0]):
+        sel = key == k
+        w[sel] = cnt[sel].max()
+    return w
+
+
 @pytest.mark.parametrize("name", ["causal_ragged", "docs_small", "window_sink_small", "random_cols_small",
                                   "random_cols_d64", "all_masked_small", "long_packing_128k",
                                   "sliding_window_sink"])
 def test_work_order_longest_first_and_stable(fm, name):
     """The plan's two work orders (read at the offsets its header records) are
-    the stable sorts, longest bucket first, of the non-skip counts of the
-    oracle's labels: per (b, hm, Q tile) for the forward and per (b, hm, KV
-    tile) for the backward, entries s * n_tiles + tile; the bucket starts
-    delimit the buckets."""
+    the stable sorts, longest bucket first, of the oracle's labels: per
+    (b, hm, Q tile) for the forward by the tile's own non-skip count, and per
+    (b, hm, KV tile) for the backward by the longest count of its group (the
+    KV tiles whose Q lists end at the same tile); entries s * n_tiles + tile;
+    the bucket starts delimit the buckets."""
     wl = W.SMALL.get(name) or W.FULL[name]
     m = W.make_mask(wl)
     att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"])
@@ -102,9 +117,10 @@ def test_work_order_longest_first_and_stable(fm, name):
     off_row, off_col, off_rb, off_cb = (int(x) for x in hdr[40:72].view(np.int64))
     ref = oracle.tile_labels_all(m, 128, 128)                  # [B, Hm, n_q, n_k]
     S = wl.B * wl.Hm
-    for cnt, off, offb, n_t in (((ref != oracle.SKIP).sum(axis=3).reshape(S * n_q), off_row, off_rb, n_q),
-                                ((ref != oracle.SKIP).sum(axis=2).reshape(S * n_k), off_col, off_cb, n_k)):
-        bkt = _bucket(cnt)
+    wrow = (ref != oracle.SKIP).sum(axis=3).reshape(S * n_q)
+    wcol = np.concatenate([_group_weights(ref[b, hm].T) for b in range(wl.B) for hm in range(wl.Hm)])
+    for wts, off, offb, n_t in ((wrow, off_row, off_rb, n_q), (wcol, off_col, off_cb, n_k)):
+        bkt = _bucket(wts)
         got = plan[off:off + 4 * S * n_t].view(np.int32)
         assert np.array_equal(got, np.argsort(bkt, kind="stable"))
         starts = plan[offb:offb + 4 * 65].view(np.int32)
