@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libfm.so")
-SOURCES = ["fm_api.cu", "fm_classify.cu", "fm_fwd.cu", "fm_bwd.cu", "fm_fp8.cu", "fm_noalloc.cu", "fm_mask.cpp"]
+SOURCES = ["fm_api.cu", "fm_classify.cu", "fm_fwd.cu", "fm_bwd.cu", "fm_fp8.cu", "fm_compress.cu", "fm_noalloc.cu", "fm_mask.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

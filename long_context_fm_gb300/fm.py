@@ -31,7 +31,8 @@ EXPORTED = ["fm_status_string", "fm_abi_version", "fm_mask_from_rows", "fm_mask_
             "fm_attn_bwd", "fm_profile_begin", "fm_profile_end", "fm_selftest_wait_timeout",
             "fm_attn_bwd_noalloc", "fm_step_graph_create", "fm_step_graph_launch", "fm_step_graph_destroy",
             "fm_plan_bytes_rows", "fm_tile_classify_rows", "fm_attn_fwd_rows", "fm_attn_bwd_rows",
-            "fm_quantize_fp8", "fm_attn_fwd_fp8", "fm_debug_wait_test"]
+            "fm_quantize_fp8", "fm_attn_fwd_fp8", "fm_debug_wait_test", "fm_bounds_compressed_bytes",
+            "fm_bounds_compress", "fm_bounds_decompress"]
 # Size of the library's built-in backward workspace (FM_NOALLOC_SCRATCH_BYTES in fm.h).
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
@@ -87,6 +88,10 @@ _lib.fm_profile_end.restype = _I
 _lib.fm_profile_end.argtypes = [_P, _I]
 _lib.fm_selftest_wait_timeout.argtypes = [ctypes.c_longlong, _P, _P]
 _lib.fm_debug_wait_test.argtypes = [ctypes.c_int, ctypes.c_longlong]
+_lib.fm_bounds_compressed_bytes.argtypes = [_P, _P, _P, _P, _I, _I, _I]
+_lib.fm_bounds_compressed_bytes.restype = _SZ
+_lib.fm_bounds_compress.argtypes = [_P, _P, _P, _P, _I, _I, _I, _P, _SZ]
+_lib.fm_bounds_decompress.argtypes = [_P, _SZ, Bounds, _P, _P]
 _lib.fm_plan_bytes_rows.restype = _SZ
 _lib.fm_plan_bytes_rows.argtypes = [_I, _I, _I, _I, _I, _I, _I]
 _lib.fm_tile_classify_rows.argtypes = [Bounds, _I, _I, _I, _I, _P, _SZ, _P, _P, _P]
@@ -273,6 +278,29 @@ def fm_profile_end(max_entries=4096):
     if n < 0:
         raise FmError(FM_ERR_CUDA, "fm_profile_end")
     return [(KERNEL_NAMES[buf[i].kernel], float(buf[i].ms)) for i in range(n)]
+
+
+def fm_bounds_compress(lts, lte, uts, ute):
+    """Host int32 [B, Hm, N] bounds -> the compressed form (numpy uint8)."""
+    arr = [np.ascontiguousarray(x, dtype=np.int32) for x in (lts, lte, uts, ute)]
+    if not all(a.shape == arr[0].shape and a.ndim == 3 for a in arr):
+        raise ValueError("bounds must be int32 [B, Hm, N], all of one shape")
+    B, Hm, N = arr[0].shape
+    p = [a.ctypes.data_as(ctypes.c_void_p) for a in arr]
+    n = _lib.fm_bounds_compressed_bytes(*p, B, Hm, N)
+    if n == 0:
+        raise FmError(FM_ERR_INVALID_ARG, "fm_bounds_compressed_bytes")
+    out = np.zeros(n, np.uint8)
+    _check(_lib.fm_bounds_compress(*p, B, Hm, N, out.ctypes.data_as(ctypes.c_void_p), n), "fm_bounds_compress")
+    return out
+
+
+def fm_bounds_decompress(cbounds, bounds: Bounds, dev_status, stream=None):
+    """Device uint8 compressed buffer -> the device int32 arrays of `bounds`."""
+    _dev(cbounds, torch.uint8, "cbounds")
+    _dev(dev_status, torch.int32, "dev_status")
+    _check(_lib.fm_bounds_decompress(_ptr(cbounds), cbounds.numel(), bounds, _ptr(dev_status), _stream(stream)),
+           "fm_bounds_decompress")
 
 
 def fm_debug_wait_test(kernel, limit_cycles):
