@@ -26,10 +26,10 @@ fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, float scale, int64_t
 fm_status fm_fwd_prepare(int d, bool precise);
 fm_status fm_fwd_prepare_fp8();
 fm_status fm_fwd_launch_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
-                            const FwdArgs &a, cudaStream_t stream);
+                            const CUtensorMap &to, const FwdArgs &a, cudaStream_t stream);
 fm_status fm_bwd_prepare(int d, bool precise);
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const FwdArgs &a, int d, bool precise, cudaStream_t stream);
+                        const CUtensorMap &to, const FwdArgs &a, int d, bool precise, cudaStream_t stream);
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                              const CUtensorMap &tdo, const BwdArgs &a, int d,
                              bool precise, cudaStream_t stream);
@@ -84,6 +84,24 @@ bool make_tmap_u8(CUtensorMap *map, const void *base, int BH, int rows, int cols
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// O, fp32 or bf16 [BH, Nq, d], viewed as 3-D (d, Nq, BH) for TMA stores: box =
+// 64 bytes (16 fp32 or 32 bf16 columns) x 32 rows, 64-byte swizzle; rows at
+// or beyond Nq are not written.
+bool make_tmap_out(CUtensorMap *map, void *base, int BH, int Nq, int d, bool f32)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t esz = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Nq, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * esz, (cuuint64_t)Nq * d * esz};
+    const cuuint32_t box[3] = {(cuuint32_t)(64 / esz), 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -287,9 +305,9 @@ fm_status fm_attn_fwd_rows(const void *q, const void *k, const void *v, fm_bound
     if (!plan_layout(B, m.Hm, N, 128, 128, &L, q_row0, Nq)) return FM_ERR_INVALID_ARG;
     if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
     if ((st = check_device()) != FM_OK) return st;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 128) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
-        !make_tmap_bf16(&tv, v, B * H, N, d, 128))
+        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_out(&to, o, B * H, Nq, d, o_dtype == FM_DT_F32))
         return FM_ERR_CUDA;
     FwdArgs a;
     a.lts = m.lts; a.lte = m.lte; a.uts = m.uts; a.ute = m.ute;
@@ -301,7 +319,7 @@ fm_status fm_attn_fwd_rows(const void *q, const void *k, const void *v, fm_bound
     a.o_f32 = o_dtype == FM_DT_F32;
     a.descale = nullptr;
     wait_test_args(0, &a.wait_limit, &a.withhold);
-    return fm_fwd_launch(tq, tk, tv, a, d, (flags & FM_FLAG_PRECISE) != 0, (cudaStream_t)stream);
+    return fm_fwd_launch(tq, tk, tv, to, a, d, (flags & FM_FLAG_PRECISE) != 0, (cudaStream_t)stream);
 }
 
 fm_status fm_attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *vt8, const float *descale,
@@ -322,9 +340,9 @@ fm_status fm_attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v
     if (!plan_layout(B, m.Hm, N, 128, 128, &L)) return FM_ERR_INVALID_ARG;
     if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
     if ((st = check_device()) != FM_OK) return st;
-    CUtensorMap tq, tk, tvt;
+    CUtensorMap tq, tk, tvt, to;
     if (!make_tmap_u8(&tq, q8, B * H, N, d, 128) || !make_tmap_u8(&tk, k8, B * H, N, d, 128) ||
-        !make_tmap_u8(&tvt, vt8, B * H, d, N, d))
+        !make_tmap_u8(&tvt, vt8, B * H, d, N, d) || !make_tmap_out(&to, o, B * H, N, d, o_dtype == FM_DT_F32))
         return FM_ERR_CUDA;
     FwdArgs a;
     a.lts = m.lts; a.lte = m.lte; a.uts = m.uts; a.ute = m.ute;
@@ -337,7 +355,7 @@ fm_status fm_attn_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v
     a.descale = descale;
     a.wait_limit = kWaitLimitCycles;
     a.withhold = 0;
-    return fm_fwd_launch_fp8(tq, tk, tvt, a, (cudaStream_t)stream);
+    return fm_fwd_launch_fp8(tq, tk, tvt, to, a, (cudaStream_t)stream);
 }
 
 fm_status fm_attn_fwd(const void *q, const void *k, const void *v, fm_bounds m, const void *plan, int B,

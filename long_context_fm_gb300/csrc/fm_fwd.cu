@@ -15,11 +15,12 @@
 // epilogue, and TMEM is allocated once per CTA.  Roles:
 //   warp 0      TMA producer of Q (per unit) and K (three-stage ring)
 //   warp 1      allocates TMEM; one thread issues the Q K^T MMAs
-//   warps 2-5   softmax, KV columns [0, 64) of every row (thread = row =
-//               TMEM lane)
-//   warps 6-9   softmax, KV columns [64, 128)
-//   warp 10     TMA producer of V (two-stage ring); stages the column bounds
-//               of partial tiles with it
+//   warps 2-5   softmax of the even tiles of the CTA-wide sequence, all 128
+//               key columns of every row (thread = row = TMEM lane); each
+//               warp turns the column bounds of its next partial tile into
+//               bit masks over its 32 rows while it waits for the scores
+//   warps 6-9   softmax of the odd tiles
+//   warp 10     TMA producer of V (two-stage ring)
 //   warp 11     one thread issues the P V MMAs
 // Two issuing threads: the scores of later tiles are issued as soon as
 // their K and score buffer are free, independently of the P V products
@@ -30,11 +31,13 @@
 // The scores of tile t + 1 are computed while the softmax works on tile t;
 // P is written as packed bf16 over the first 64 columns of its S buffer (the
 // A operand of O += P V), and the buffer is reused by the scores of tile
-// t + 3 once that PV has read it.  The two softmax warpgroups exchange their
-// row maxima through shared memory at a named barrier of their 256 threads
-// (every thread of both reaches it on every tile, also after an abort, so it
-// always completes), take the same lazy-rescale decision, and each rescales
-// and finally stores its half of O's columns.
+// t + 3 once that PV has read it.  The two softmax warpgroups take
+// alternate tiles, so one's TMEM loads, waits and row max overlap the other's
+// exponentials; the running row max passes from each tile's owner to the
+// next through shared memory (a producer / consumer named barrier per
+// direction, reached on every tile, also after an abort).  The owner of a
+// tile that raises the max rescales O; each warpgroup keeps its own sum of P,
+// and the epilogue combines the two and each stores half of O's columns.
 // Precise mode: P = P_hi + P_lo (P_lo = bf16(P - bf16(P))) in columns
 // [0, 64) and [64, 128) of the S buffer, both multiplied by V.
 // Online softmax in the base-2 domain with a lazy rescale: O and l are
@@ -54,7 +57,6 @@ enum {
     FB_Q = 0,
     FB_KF0, FB_KF1, FB_KF2, FB_KE0, FB_KE1, FB_KE2,   // K stage loaded / released
     FB_VF0, FB_VF1, FB_VE0, FB_VE1,                   // V stage loaded / released
-    FB_BF0, FB_BF1,                                   // bounds of the V stage's tile staged
     FB_S0, FB_S1, FB_S2,                              // scores of buffer b computed
     FB_P0, FB_P1, FB_P2,                              // P of buffer b written (both warpgroups)
     FB_O0, FB_O1, FB_O2,                              // O += P V of a tile using buffer b completed
@@ -74,18 +76,36 @@ struct FwdSmem {
     static constexpr int kQ = 0;
     static constexpr int kK = kTile;                           // [kKStages]
     static constexpr int kV = kK + kKStages * kTile;           // [kVStages]
-    static constexpr int kBnd = kV + kVStages * kTile;         // int4 [kVStages][128]
-    static constexpr int kMax = kBnd + kVStages * 128 * 16;    // float [2 slots][2 warpgroups][128]
+    static constexpr int kOst = kV + kVStages * kTile;         // O staging: [8 softmax warps][32 rows][64 bytes]
+    static constexpr int kMask = kOst + 8 * 2048;              // uint32 [8 softmax warps][2 buffers][128 columns]
+    static constexpr int kMax = kMask + 8 * 2 * 128 * 4;       // float [2 slots][2 warpgroups][128]: final m
     static constexpr int kSum = kMax + 2 * 2 * 128 * 4;        // float [2 slots][2 warpgroups][128]: l
     static constexpr int kUnit = kSum + 2 * 2 * 128 * 4;       // int4 [4]: unit ring (qt, bh, sidx, n)
     static constexpr int kFlag = kUnit + 4 * 16;               // int [2][8]: softmax warps' unit decisions
-    static constexpr int kBar = kFlag + 16 * 4;
+    static constexpr int kChain = kFlag + 16 * 4;              // float [128]: running row max handed between warpgroups
+    static constexpr int kBar = kChain + 128 * 4;
     static constexpr int kNumBar = FB_COUNT;
     static constexpr int kMisc = kBar + kNumBar * 8;
     // At least 120 KB so that one CTA (512 TMEM columns) is resident per SM.
     static constexpr int kBytes = (kMisc + 64 > 120 * 1024) ? kMisc + 64 : 120 * 1024;
 };
 
+
+// Bits x of a 32-row group with lo <= x < hi (bounds clamped to [0, 32]).
+__device__ __forceinline__ uint32_t row_bits32(int lo, int hi)
+{
+    lo = min(max(lo, 0), 32);
+    hi = min(max(hi, 0), 32);
+    if (hi <= lo) return 0u;
+    return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
+}
+
+// fp32 bits x, or -inf where bit (31 - sh) of `word` is set.
+__device__ __forceinline__ uint32_t neg_inf_where(uint32_t x, uint32_t word, uint32_t sh)
+{
+    const uint32_t m = (uint32_t)((int32_t)(word << sh) >> 31);
+    return (x & ~m) | (0xff800000u & m);
+}
 
 constexpr int kSB = 3;              // score buffers in TMEM
 constexpr int kUnitRing = 4;        // claimed units buffered between the K producer and the other roles
@@ -97,11 +117,19 @@ constexpr int kUnitReaders = 11;    // V producer, two MMA issuers, eight softma
 constexpr int kFwdSchedSlots = 64;
 static __device__ unsigned int g_fwd_sched[kFwdSchedSlots][2];
 constexpr int kSoftmaxBar = 1;      // named barrier of the two softmax warpgroups (256 threads)
+// Register budgets (setmaxnreg): the four warps that issue copies or MMAs
+// give registers to the eight softmax warps (128 scores each in registers);
+// together they use the 384 x 168 registers the block launches with, which
+// the host checks against the compiled kernel.
+constexpr int kFwdLaunchRegs = 168;
+constexpr int kRegsIssue = 56, kRegsSoftmax = 224;
+static_assert(4 * 32 * kRegsIssue + 8 * 32 * kRegsSoftmax <= 384 * kFwdLaunchRegs, "register split of the forward");
+constexpr int kChainBar = 2;        // 2 + w: row max handed on by warpgroup w (arrive) to the other (sync)
 
 template <int D, bool PRECISE, bool FP8>
 __global__ void __launch_bounds__(384, 1)
     fm_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const FwdArgs a)
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, const FwdArgs a)
 {
     static_assert(!(PRECISE && FP8), "the FP8 path has no precise mode");
     static_assert(!FP8 || D == 128, "the FP8 path is built for d = 128");
@@ -115,7 +143,7 @@ __global__ void __launch_bounds__(384, 1)
     // instruction rather than a generic one.
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;
-    int4 *sBnd = reinterpret_cast<int4 *>(smem + S::kBnd);
+    uint32_t *sMask = reinterpret_cast<uint32_t *>(smem + S::kMask);
     float *sMax = reinterpret_cast<float *>(smem + S::kMax);
     float *sSum = reinterpret_cast<float *>(smem + S::kSum);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kBar);
@@ -147,13 +175,12 @@ __global__ void __launch_bounds__(384, 1)
             for (int s = 0; s < VS; ++s) {
                 mbar_init(&bars[FB_VF0 + s], 1);
                 mbar_init(&bars[FB_VE0 + s], 1);
-                mbar_init(&bars[FB_BF0 + s], 32);
             }
             // One O barrier per score buffer: the PV of tile g commits to O_{g mod 3},
             // so every wait below targets a barrier at most one phase behind.
             for (int s = 0; s < kSB; ++s) {
                 mbar_init(&bars[FB_S0 + s], 1);
-                mbar_init(&bars[FB_P0 + s], 256);
+                mbar_init(&bars[FB_P0 + s], 128);   // the tile's softmax warpgroup
                 mbar_init(&bars[FB_O0 + s], 1);
             }
             for (int s = 0; s < kUnitRing; ++s) {
@@ -231,6 +258,7 @@ __global__ void __launch_bounds__(384, 1)
 
     if (*ok_sh) {
         if (warp == 0) {
+            warp_regs_dec<kRegsIssue>();
             // ------------------------------------------------ K producer
             // Per unit with tiles: Q (once the previous unit's last scores have
             // read the Q buffer), then K through its ring: K of tile g is loaded
@@ -299,10 +327,10 @@ __global__ void __launch_bounds__(384, 1)
                     if (k2 != withheld) mbar_wait_drain(&bars[FB_KF0 + (k2 % KS)], (k2 / KS) & 1, a.status, a.wait_limit);
             }
         } else if (warp == 10) {
+            warp_regs_dec<kRegsIssue>();
             // ------------------------------------------------ V producer
-            // V through its ring, and the column bounds of partial tiles staged with
-            // it: the V stage (and its bounds) is free once the PV of tile g - VS
-            // has completed, which follows the softmax's use of those bounds.
+            // V through its ring: the stage of tile g is free once the PV of tile
+            // g - VS has completed.
             if (lane == 0) tma_prefetch_desc(&tv);
             int g = 0;    // V loads begun (CTA-wide tile counter)
             bool run = true;
@@ -315,23 +343,7 @@ __global__ void __launch_bounds__(384, 1)
                     const int e = e_next;
                     if (t + 1 < u.n) e_next = u.list[t + 1];
                     const int kb = (e & kTileMask) * 128;
-                    const bool pred = ((e >> kLabelShift) == FM_TILE_PARTIAL) || kb + 128 > N;
                     const int vs = g % VS;
-                    // Column bounds of a partial tile, loaded before the wait below so
-                    // their latency overlaps it; stored as (start, length) pairs,
-                    // columns beyond N masked for every row.
-                    int4 bv[4];
-                    if (pred) {
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int j = kb + lane * 4 + w;
-                            bv[w] = make_int4(0, 0, 0, 0x7fffffff);
-                            if (j < N) {
-                                const int64_t o = (int64_t)u.sidx * N + j;
-                                bv[w] = make_int4(a.lts[o], a.lte[o], a.uts[o], a.ute[o]);
-                            }
-                        }
-                    }
                     if (g >= VS && !warp_wait(&bars[FB_VE0 + vs], ((g / VS) - 1) & 1, abort, a.status, a.wait_limit)) {
                         run = false;
                         break;
@@ -345,22 +357,13 @@ __global__ void __launch_bounds__(384, 1)
                             for (int x = 0; x < NBOX; ++x)
                                 tma_load_3d(smem + S::kV + vs * S::kTile + x * S::kBox, &tv, &bars[FB_VF0 + vs], x * 64, kb, u.bh);
                     }
-                    if (pred) {
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int4 v = bv[w];
-                            sBnd[vs * 128 + lane * 4 + w] = (kb + lane * 4 + w < N)
-                                                                ? make_int4(v.x, max(v.y - v.x, 0), v.z, max(v.w - v.z, 0))
-                                                                : v;
-                        }
-                    }
-                    mbar_arrive(&bars[FB_BF0 + vs]);
                 }
             }
             if (lane == 0 && *abort)
                 for (int k2 = (g > VS ? g - VS : 0); k2 < g; ++k2)
                     mbar_wait_drain(&bars[FB_VF0 + (k2 % VS)], (k2 / VS) & 1, a.status, a.wait_limit);
         } else if (warp == 1) {
+            warp_regs_dec<kRegsIssue>();
             // ------------------------------------------------ S issuer
             // The scores of tile g as soon as its unit's Q and its K have landed and
             // its score buffer has been read by the PV of tile g - 3; runs ahead of
@@ -414,6 +417,7 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_wait_drain(&bars[FB_DRAIN], 0, a.status, a.wait_limit);
             }
         } else if (warp == 11) {
+            warp_regs_dec<kRegsIssue>();
             // ------------------------------------------------ PV issuer
             // O += P V of tile g once the softmax has written P and V has landed; the
             // first PV of a unit overwrites O, so it waits until the previous unit's
@@ -465,15 +469,30 @@ __global__ void __launch_bounds__(384, 1)
                 mbar_wait_drain(&bars[FB_DRAIN], 0, a.status, a.wait_limit);
             }
         } else {
+            warp_regs_inc<kRegsSoftmax>();
             // ------------------------------------------------ softmax (warps 2-9)
-            const int w = (warp < 6) ? 0 : 1;          // column half: KV columns [64 w, 64 w + 64)
+            // Tile g of the CTA-wide sequence belongs to warpgroup g & 1 (warps 2-5
+            // or 6-9; each covers all 128 TMEM lanes), which handles every key
+            // column of its rows: thread = row = TMEM lane, 128 scores in registers.
+            // The two warpgroups work on consecutive tiles at the same time, so the
+            // TMEM loads, waits and row max of one overlap the exponentials of the
+            // other.  Only the running row max passes from one tile to the next:
+            // the owner of tile t > 0 of a unit takes the max in force after tile
+            // t - 1 from the other warpgroup, decides its own and hands it on
+            // before it computes its exponentials.  When the max rises the owner
+            // rescales all of O once the P V of tile t - 1 has completed, before it
+            // releases its own P; the P V products then accumulate in tile order.
+            // Each warpgroup sums its own P relative to the max it last used; the
+            // epilogue combines the two sums.
+            const int w = (warp < 6) ? 0 : 1;          // warpgroup: owns the tiles g with g & 1 == w
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             const uint32_t tO = tmem + 384;
-            constexpr int OC = D / 2;                  // O columns rescaled / stored by this warpgroup
+            constexpr int OC = D / 2;                  // O columns stored by this warpgroup
             // softmax scale * log2(e), with the Q and K descales on the FP8 path
             const float sl2 = FP8 ? a.scale_log2 * a.descale[0] * a.descale[1] : a.scale_log2;
+            volatile float *sChain = reinterpret_cast<volatile float *>(smem + S::kChain);
             // `live` turns false (for the whole warp) when a wait gives up after an
             // abort; the warp then skips its work but still reaches every named
             // barrier of the loop, so the other warpgroup is never left waiting.
@@ -482,8 +501,48 @@ __global__ void __launch_bounds__(384, 1)
             auto wait_pv = [&](int k) {
                 live = live && warp_wait(&bars[FB_O0 + k % kSB], (k / kSB) & 1, abort, a.status, a.wait_limit);
             };
-            int g = 0;     // tiles begun (CTA-wide)
+            int g = 0;     // tiles begun (CTA-wide, both warpgroups)
             int nu = 0;    // units with tiles finished
+            int nbf = 0;   // this warpgroup's partial tiles (their masks alternate between two buffers)
+            uint32_t *sMaskW = sMask + (warp - 2) * 256;   // this warp's two mask buffers
+            // The mask of a partial tile as bits over this warp's 32 rows of the Q
+            // tile (mask rows r0 + 32 quarter + x): word c has bit x set when that
+            // row lies in [lts, lte) or [uts, ute) of the tile's column c; columns
+            // beyond N are masked in every row.  Lane j covers columns 4 j .. 4 j + 3.
+            // Built by the warp itself between its tiles, read back by all its lanes:
+            // the bounds are loaded one tile ahead (load_bounds at the start of the
+            // warpgroup's previous tile) and turned into bits after that tile's P
+            // is released (build_mask).
+            int4 bnd[4];
+            auto load_bounds = [&](int e, const Unit &uu) {
+                const int kb = (e & kTileMask) * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = kb + lane * 4 + c;
+                    bnd[c] = make_int4(0, 0, 0, 0);
+                    if (j < N) {
+                        const int64_t o = (int64_t)uu.sidx * N + j;
+                        bnd[c] = make_int4(a.lts[o], a.lte[o], a.uts[o], a.ute[o]);
+                    }
+                }
+            };
+            auto build_mask = [&](int e, const Unit &uu, uint32_t *dst) {
+                const int kb = (e & kTileMask) * 128;
+                const int base = a.q_row0 + uu.qt * 128 + quarter * 32;
+                uint32_t wq[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int4 v = bnd[c];
+                    wq[c] = (kb + lane * 4 + c < N)
+                                ? (row_bits32(v.x - base, v.y - base) | row_bits32(v.z - base, v.w - base))
+                                : 0xffffffffu;
+                }
+                *reinterpret_cast<uint4 *>(dst + lane * 4) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                __syncwarp();
+            };
+            auto is_partial = [&](int e) {
+                return ((e >> kLabelShift) == FM_TILE_PARTIAL) || (e & kTileMask) * 128 + 128 > N;
+            };
             Unit un;
             for (int k = 0;; ++k) {
                 // Both warpgroups take the same decision on every unit: a wait that
@@ -497,138 +556,161 @@ __global__ void __launch_bounds__(384, 1)
                 for (int q = 1; q < 8; ++q) all &= sFlag[(k & 1) * 8 + q];
                 if (!all) break;
                 const int li = un.qt * 128 + r;            // row of Q / O / lse
-                const int i = a.q_row0 + li;               // row of the mask
-                float m = -INFINITY, l = 0.f;
-                int e_next = un.n > 0 ? un.list[0] : 0;
-                for (int t = 0; t < un.n; ++t, ++g) {
+                float m = -INFINITY;   // the max this warpgroup last used (scaled, base 2)
+                float l = 0.f;         // this warpgroup's sum of P, relative to m
+                const int g0 = g;
+                const int t0 = (w - g0) & 1;               // this warpgroup's first tile of the unit
+                int e_next = t0 < un.n ? un.list[t0] : 0;
+                if (live && t0 < un.n && is_partial(e_next)) {
+                    load_bounds(e_next, un);
+                    build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
+                }
+                for (int t = t0; t < un.n; t += 2) {
+                    const int gt = g0 + t;
                     const int e = e_next;
-                    if (t + 1 < un.n) e_next = un.list[t + 1];
+                    if (t + 2 < un.n) e_next = un.list[t + 2];
+                    const bool next_pred = t + 2 < un.n && is_partial(e_next);
+                    if (live && next_pred) load_bounds(e_next, un);   // consumed after this tile's P
                     const int kb = (e & kTileMask) * 128;
                     const bool pred = ((e >> kLabelShift) == FM_TILE_PARTIAL) || kb + 128 > N;
-                    const int bb = g % kSB, vs = g % VS;
+                    const int bb = gt % kSB;
                     const uint32_t tS = tmem + bb * 128;
-                    live = live && warp_wait(&bars[FB_S0 + bb], (g / kSB) & 1, abort, a.status, a.wait_limit);
-                    live = live && (!pred || warp_wait(&bars[FB_BF0 + vs], (g / VS) & 1, abort, a.status, a.wait_limit));
-                    float sv[64];
-                    float mxl = -INFINITY;
+                    live = live && warp_wait(&bars[FB_S0 + bb], (gt / kSB) & 1, abort, a.status, a.wait_limit);
+                    uint32_t sv[128];                      // the row's scores (fp32 bits)
+                    float mx = -INFINITY;
+                    const uint4 *mk = reinterpret_cast<const uint4 *>(sMaskW + (nbf & 1) * 128);
+                    if (pred) ++nbf;
                     if (live) {
                         tc_fence_after();
-                        uint32_t raw[2][32];
-                        tmem_ld32(tS + lane_off + w * 64, raw[0]);
-                        tmem_ld32(tS + lane_off + w * 64 + 32, raw[1]);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            tmem_ld32(tS + lane_off + c * 32, reinterpret_cast<uint32_t (&)[32]>(sv[c * 32]));
                         tmem_ld_wait();
-                        tmem_reg_fence(raw[0]);
-                        tmem_reg_fence(raw[1]);
-#pragma unroll
-                        for (int cc = 0; cc < 64; ++cc) sv[cc] = __uint_as_float(raw[cc >> 5][cc & 31]);
+                        tmem_reg_fence(sv);
                         if (pred) {
-                            const int4 *bnd = sBnd + vs * 128 + w * 64;
+                            // The lane is the bit of its row; masked scores become -inf.
+                            const uint32_t sh = 31u - (uint32_t)lane;
 #pragma unroll
-                            for (int cc = 0; cc < 64; ++cc) {
-                                const int4 x = bnd[cc];
-                                const bool msk = ((unsigned)(i - x.x) < (unsigned)x.y) || ((unsigned)(i - x.z) < (unsigned)x.w);
-                                sv[cc] = msk ? -INFINITY : sv[cc];
+                            for (int c4 = 0; c4 < 32; ++c4) {
+                                const uint4 mw = mk[c4];
+                                sv[4 * c4 + 0] = neg_inf_where(sv[4 * c4 + 0], mw.x, sh);
+                                sv[4 * c4 + 1] = neg_inf_where(sv[4 * c4 + 1], mw.y, sh);
+                                sv[4 * c4 + 2] = neg_inf_where(sv[4 * c4 + 2], mw.z, sh);
+                                sv[4 * c4 + 3] = neg_inf_where(sv[4 * c4 + 3], mw.w, sh);
                             }
                         }
-                        float mx4[4] = {sv[0], sv[1], sv[2], sv[3]};
+                        float mx4[4] = {__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]),
+                                        __uint_as_float(sv[3])};
 #pragma unroll
-                        for (int k2 = 0; k2 < 30; ++k2) mx4[k2 & 3] = fmax3(mx4[k2 & 3], sv[4 + 2 * k2], sv[5 + 2 * k2]);
-                        mxl = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                        for (int k2 = 0; k2 < 62; ++k2)
+                            mx4[k2 & 3] = fmax3(mx4[k2 & 3], __uint_as_float(sv[4 + 2 * k2]), __uint_as_float(sv[5 + 2 * k2]));
+                        mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;   // -inf stays -inf
                     }
-                    // Row max over both column halves.  Both warpgroups hold their S
-                    // columns in registers once the barrier completes, so P may then
-                    // overwrite the S buffer.
-                    const int slot = g & 1;
-                    sMax[(slot * 2 + w) * 128 + r] = mxl;
-                    tc_fence_before();
-                    named_bar_sync(kSoftmaxBar, 256);
-                    tc_fence_after();
+                    // The max in force after tile t - 1, this tile's decision, and the
+                    // hand-over to the owner of tile t + 1 (named barrier kChainBar + the
+                    // producer's warpgroup: bar.arrive by the producer, bar.sync by the
+                    // consumer).  Both sides depend only on t and n, so they stay
+                    // matched on every tile, also after an abort.
+                    float m_prev = -INFINITY;
+                    if (t > 0) {
+                        named_bar_sync(kChainBar + (1 - w), 256);
+                        m_prev = sChain[r];
+                    }
+                    const float m_new = (mx > m_prev + 8.f) ? mx : m_prev;
+                    if (t + 1 < un.n) {
+                        sChain[r] = m_new;
+                        named_bar_arrive(kChainBar + w, 256);
+                    }
                     if (!live) continue;
-                    const float mx = fmaxf(mxl, sMax[(slot * 2 + (1 - w)) * 128 + r]) * sl2;   // -inf stays -inf
-                    float m_new = m, alpha = 1.f;
-                    if (mx > m + 8.f) {
-                        m_new = mx;
-                        alpha = ex2(m - m_new);                  // m = -inf gives 0
-                    }
-                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-                    // Rescale this warpgroup's half of O when the max moved (rare with
-                    // the 2^8 threshold); the PV of the previous tile must be complete.
-                    if (__any_sync(0xffffffffu, t > 0 && alpha != 1.f)) {
-                        wait_pv(g - 1);
+                    // O holds tiles 0 .. t - 1 relative to m_prev: rescale it when the
+                    // max rose (rare with the 2^8 threshold), after their P V completed.
+                    if (__any_sync(0xffffffffu, t > 0 && m_new != m_prev)) {
+                        const float alpha = (m_new != m_prev) ? ex2(m_prev - m_new) : 1.f;   // m_prev = -inf gives 0
+                        wait_pv(gt - 1);
                         if (!live) continue;
                         tc_fence_after();
 #pragma unroll
-                        for (int cc = 0; cc < OC / 32; ++cc) {
-                            uint32_t ov[32];
-                            tmem_ld32(tO + lane_off + w * OC + cc * 32, ov);
+                        for (int cc = 0; cc < D / 16; ++cc) {
+                            uint32_t ov[16];
+                            tmem_ld16(tO + lane_off + cc * 16, ov);
                             tmem_ld_wait();
                             tmem_reg_fence(ov);
 #pragma unroll
-                            for (int u = 0; u < 32; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * alpha);
-                            tmem_st32(tO + lane_off + w * OC + cc * 32, ov);
+                            for (int u = 0; u < 16; ++u) ov[u] = __float_as_uint(__uint_as_float(ov[u]) * alpha);
+                            tmem_st16(tO + lane_off + cc * 16, ov);
                         }
                     }
-                    // P = exp2(s * scale*log2e - m) as packed bf16 over the S buffer:
-                    // this warpgroup's 64 columns go to TMEM columns [32 w, 32 w + 32)
-                    // (precise mode: P_lo to [64 + 32 w, ...)).  O is normalised by the
+                    // P = exp2(s * scale*log2e - m) as packed bf16 over the first 64
+                    // columns of the S buffer (precise mode: P_lo over the next 64; FP8:
+                    // four e4m3 per column over the first 32).  O is normalised by the
                     // fp32 sum of P, which also gives lse (standard mode: the bf16
                     // rounding of the weights P V applied moves that sum by ~2^-9
-                    // relative at most, far inside the tolerance, and summing the
-                    // rounded values instead costs 1.5 instructions per element on
-                    // the critical chain).  Column pairs in packed fp32.
+                    // relative at most, far inside the tolerance).  Column pairs in
+                    // packed fp32.
+                    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                     const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_use, -m_use);
-                    uint32_t f8[16];          // FP8: the warpgroup's 64 P values, 4 e4m3 per column
+                    uint32_t f8[32];          // FP8: the row's 128 P values, 4 e4m3 per column
                     uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < 4; ++hh) {          // 32 keys per step
                         uint32_t hi[16], lo[16];
 #pragma unroll
                         for (int cc = 0; cc < 16; ++cc) {
                             float x0, x1;
-                            f2_unpack(f2_fma(f2_pack(sv[hh * 32 + 2 * cc], sv[hh * 32 + 2 * cc + 1]), sc2, nm2), x0, x1);
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[hh * 32 + 2 * cc]), __uint_as_float(sv[hh * 32 + 2 * cc + 1])),
+                                             sc2, nm2),
+                                      x0, x1);
                             const float p0 = ex2(x0), p1 = ex2(x1);
                             sum2 = f2_add(sum2, f2_pack(p0, p1));
-                            hi[cc] = pack_bf16x2(p0, p1);
                             if (FP8) {
-                                const uint32_t e2 = pack_e4m3x2(p0, p1);     // columns 2 cc, 2 cc + 1
+                                const uint32_t e2 = pack_e4m3x2(p0, p1);     // keys hh*32 + 2 cc, + 1
                                 if (cc & 1) f8[hh * 8 + (cc >> 1)] |= e2 << 16;
                                 else f8[hh * 8 + (cc >> 1)] = e2;
-                            }
-                            if (PRECISE) {
-                                lo[cc] = pack_bf16x2(p0 - __uint_as_float(hi[cc] << 16),
-                                                     p1 - __uint_as_float(hi[cc] & 0xffff0000u));
+                            } else {
+                                hi[cc] = pack_bf16x2(p0, p1);
+                                if (PRECISE)
+                                    lo[cc] = pack_bf16x2(p0 - __uint_as_float(hi[cc] << 16),
+                                                         p1 - __uint_as_float(hi[cc] & 0xffff0000u));
                             }
                         }
-                        if (!FP8) tmem_st16(tS + lane_off + w * 32 + hh * 16, hi);
-                        if (PRECISE) tmem_st16(tS + lane_off + 64 + w * 32 + hh * 16, lo);
+                        if (!FP8) tmem_st16(tS + lane_off + hh * 16, hi);
+                        if (PRECISE) tmem_st16(tS + lane_off + 64 + hh * 16, lo);
                     }
-                    if (FP8) tmem_st16(tS + lane_off + w * 16, f8);   // columns [16 w, 16 w + 16)
+                    if (FP8) tmem_st32(tS + lane_off, f8);
                     float s0, s1;
                     f2_unpack(sum2, s0, s1);
-                    l = l * alpha + (s0 + s1);
+                    l = (m == m_new ? l : l * ex2(m - m_new)) + (s0 + s1);
                     m = m_new;
                     tmem_st_wait();
                     tc_fence_before();
                     mbar_arrive(&bars[FB_P0 + bb]);
+                    // The mask of this warpgroup's next tile, while it waits for its scores.
+                    if (next_pred) build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
                 }
+                g = g0 + un.n;
                 // ------------------------------------------------ epilogue
-                // Combine the two warpgroups' partial sums (one more named barrier,
-                // reached by every thread of both; the slot alternates between
-                // units), then each stores its half of O after the last PV.  O is
-                // released to the next unit's first PV as soon as it is in
-                // registers.  A unit without tiles writes O = 0, lse = -inf.
+                // Combine the two warpgroups' sums at the final max, the larger of
+                // the two they last used (one more named barrier, reached by every
+                // thread of both; the slot alternates between units), then each
+                // stores its half of O's columns after the last PV.  O is released to
+                // the next unit's first PV as soon as it is in registers.  A unit
+                // without tiles writes O = 0, lse = -inf.
                 const int su = nu & 1;
                 if (un.n > 0) {
                     sSum[(su * 2 + w) * 128 + r] = l;
+                    sMax[(su * 2 + w) * 128 + r] = m;
                     named_bar_sync(kSoftmaxBar, 256);
                     wait_pv(g - 1);
                 }
                 if (live) {
                     uint32_t ov[OC];
-                    float lt = 0.f;
+                    float lt = 0.f, mf = -INFINITY;
                     if (un.n > 0) {
                         tc_fence_after();
-                        lt = sSum[(su * 2) * 128 + r] + sSum[(su * 2 + 1) * 128 + r];
+                        const float m0 = sMax[(su * 2) * 128 + r], m1 = sMax[(su * 2 + 1) * 128 + r];
+                        const float l0 = sSum[(su * 2) * 128 + r], l1 = sSum[(su * 2 + 1) * 128 + r];
+                        mf = fmaxf(m0, m1);   // l_w > 0 implies a finite m_w <= mf
+                        lt = (l0 > 0.f ? l0 * ex2(m0 - mf) : 0.f) + (l1 > 0.f ? l1 * ex2(m1 - mf) : 0.f);
 #pragma unroll
                         for (int cc = 0; cc < OC / 32; ++cc)
                             tmem_ld32(tO + lane_off + w * OC + cc * 32, reinterpret_cast<uint32_t (&)[32]>(ov[cc * 32]));
@@ -641,36 +723,62 @@ __global__ void __launch_bounds__(384, 1)
                         for (int c = 0; c < OC; ++c) ov[c] = 0u;
                     }
                     const float inv = (lt > 0.f) ? (FP8 ? a.descale[2] : 1.f) / lt : 0.f;
-                    const bool row_in = li < a.Nq;
-                    const int64_t row = (int64_t)un.bh * a.Nq + li;
-                    if (row_in) {
+                    // O leaves through shared memory and TMA stores: the warp stages
+                    // its 32 rows x 64 bytes (16 fp32 or 32 bf16 columns) at a time in
+                    // a buffer of its own with the 64-byte swizzle (16-byte chunk q of
+                    // row x at chunk q ^ ((x >> 1) & 3): conflict-free), and the copy
+                    // engine writes whole row segments and drops rows at or beyond
+                    // Nq.  A buffer is rewritten once the previous store has read it.
+                    uint8_t *stg = smem + S::kOst + (warp - 2) * 2048;
+                    const int y0 = un.qt * 128 + quarter * 32;
+                    auto stage_store = [&](const uint4 (&pk)[4], int x) {
+                        if (lane == 0) bulk_wait_read_all();
+                        __syncwarp();
 #pragma unroll
-                        for (int cc = 0; cc < OC / 32; ++cc) {
-                            const int col = w * OC + cc * 32;
-                            const uint32_t *oc = ov + cc * 32;
-                            if (a.o_f32) {
-                                float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.o) + row * D + col);
-#pragma unroll
-                                for (int q4 = 0; q4 < 8; ++q4)
-                                    dst[q4] = make_float4(__uint_as_float(oc[4 * q4]) * inv, __uint_as_float(oc[4 * q4 + 1]) * inv,
-                                                          __uint_as_float(oc[4 * q4 + 2]) * inv, __uint_as_float(oc[4 * q4 + 3]) * inv);
-                            } else {
-                                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(a.o) + row * D + col);
-#pragma unroll
-                                for (int q8 = 0; q8 < 4; ++q8)
-                                    dst[q8] = make_uint4(pack_bf16x2(__uint_as_float(oc[8 * q8 + 0]) * inv, __uint_as_float(oc[8 * q8 + 1]) * inv),
-                                                         pack_bf16x2(__uint_as_float(oc[8 * q8 + 2]) * inv, __uint_as_float(oc[8 * q8 + 3]) * inv),
-                                                         pack_bf16x2(__uint_as_float(oc[8 * q8 + 4]) * inv, __uint_as_float(oc[8 * q8 + 5]) * inv),
-                                                         pack_bf16x2(__uint_as_float(oc[8 * q8 + 6]) * inv, __uint_as_float(oc[8 * q8 + 7]) * inv));
-                            }
+                        for (int q = 0; q < 4; ++q) st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), pk[q]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&to, stg, x, y0, un.bh);
+                            bulk_commit();
                         }
-                        if (w == 0) a.lse[row] = (lt > 0.f) ? (m + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
+                    };
+                    if (a.o_f32) {
+#pragma unroll
+                        for (int c = 0; c < OC / 16; ++c) {
+                            uint4 pk[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                pk[q] = make_uint4(__float_as_uint(__uint_as_float(ov[c * 16 + 4 * q]) * inv),
+                                                   __float_as_uint(__uint_as_float(ov[c * 16 + 4 * q + 1]) * inv),
+                                                   __float_as_uint(__uint_as_float(ov[c * 16 + 4 * q + 2]) * inv),
+                                                   __float_as_uint(__uint_as_float(ov[c * 16 + 4 * q + 3]) * inv));
+                            stage_store(pk, w * OC + c * 16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < OC / 32; ++c) {
+                            uint4 pk[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const uint32_t *oc = ov + c * 32 + 8 * q;
+                                pk[q] = make_uint4(pack_bf16x2(__uint_as_float(oc[0]) * inv, __uint_as_float(oc[1]) * inv),
+                                                   pack_bf16x2(__uint_as_float(oc[2]) * inv, __uint_as_float(oc[3]) * inv),
+                                                   pack_bf16x2(__uint_as_float(oc[4]) * inv, __uint_as_float(oc[5]) * inv),
+                                                   pack_bf16x2(__uint_as_float(oc[6]) * inv, __uint_as_float(oc[7]) * inv));
+                            }
+                            stage_store(pk, w * OC + c * 32);
+                        }
                     }
+                    if (w == 0 && li < a.Nq)
+                        a.lse[(int64_t)un.bh * a.Nq + li] = (lt > 0.f) ? (mf + __log2f(lt)) * 0.69314718055994531f : -INFINITY;
                 } else if (un.n > 0) {
                     mbar_arrive(&bars[FB_OE]);   // after an abort: nothing reads O any more
                 }
                 if (un.n > 0) ++nu;
             }
+            // Every TMA store of O has completed before the CTA leaves.
+            if (lane == 0) bulk_wait_all();
         }
     }
     tc_fence_before();
@@ -706,6 +814,11 @@ static bool fwd_smem_ready()
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load(std::memory_order_acquire)) return true;
+    // The warps' register budgets add up to the launch allocation only if the
+    // kernel was compiled to exactly kFwdLaunchRegs per thread.
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fm_fwd_kernel<D, PRECISE, FP8>) != cudaSuccess || fa.numRegs != kFwdLaunchRegs)
+        return false;
     if (cudaFuncSetAttribute(fm_fwd_kernel<D, PRECISE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
         return false;
@@ -715,7 +828,7 @@ static bool fwd_smem_ready()
 
 template <int D, bool PRECISE, bool FP8 = false>
 static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            const FwdArgs &a, cudaStream_t stream)
+                            const CUtensorMap &to, const FwdArgs &a, cudaStream_t stream)
 {
     constexpr int smem = FwdSmem<D, FP8>::kBytes;
     if (!fwd_smem_ready<D, PRECISE, FP8>()) return FM_ERR_CUDA;
@@ -729,7 +842,7 @@ static fm_status launch_fwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
     FwdArgs args = a;
     args.sched_slot = (int)(next_slot.fetch_add(1, std::memory_order_relaxed) % kFwdSchedSlots);
     ProfScope ps(kKFwd, stream);
-    fm_fwd_kernel<D, PRECISE, FP8><<<grid, 384, smem, stream>>>(tq, tk, tv, args);
+    fm_fwd_kernel<D, PRECISE, FP8><<<grid, 384, smem, stream>>>(tq, tk, tv, to, args);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
@@ -747,15 +860,16 @@ fm_status fm_fwd_prepare_fp8()
 }
 
 fm_status fm_fwd_launch_fp8(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tvt,
-                            const FwdArgs &a, cudaStream_t stream)
+                            const CUtensorMap &to, const FwdArgs &a, cudaStream_t stream)
 {
-    return launch_fwd<128, false, true>(tq, tk, tvt, a, stream);
+    return launch_fwd<128, false, true>(tq, tk, tvt, to, a, stream);
 }
 
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const FwdArgs &a, int d, bool precise, cudaStream_t stream)
+                        const CUtensorMap &to, const FwdArgs &a, int d, bool precise, cudaStream_t stream)
 {
     if (d == 128)
-        return precise ? launch_fwd<128, true>(tq, tk, tv, a, stream) : launch_fwd<128, false>(tq, tk, tv, a, stream);
-    return precise ? launch_fwd<64, true>(tq, tk, tv, a, stream) : launch_fwd<64, false>(tq, tk, tv, a, stream);
+        return precise ? launch_fwd<128, true>(tq, tk, tv, to, a, stream)
+                       : launch_fwd<128, false>(tq, tk, tv, to, a, stream);
+    return precise ? launch_fwd<64, true>(tq, tk, tv, to, a, stream) : launch_fwd<64, false>(tq, tk, tv, to, a, stream);
 }

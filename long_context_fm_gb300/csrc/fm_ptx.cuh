@@ -150,6 +150,32 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Register budget of the calling warp (setmaxnreg, warp-wide): roles that
+// only issue copies or MMAs give registers back to the block's pool and the
+// softmax warps take them.  An increase waits until the pool holds enough, so
+// the budgets of all warps must add up to at most the block's launch
+// allocation (threads x registers per thread), which the host checks against
+// the compiled kernel before it launches one.
+template <int N>
+__device__ __forceinline__ void warp_regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void warp_regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Signals a named barrier without waiting for it: the producer side of a
+// producer / consumer pair whose consumer threads call named_bar_sync with
+// the same count.  Shared-memory writes made before it are visible to the
+// consumers once their bar.sync returns.
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Generic-proxy writes to shared memory made visible to the async proxy
 // (tensor core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -174,6 +200,42 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
         : "memory");
+}
+
+// 3-D tiled store from shared memory (bulk async group of the issuing thread).
+// Elements of the box outside the tensor are not written.  Callers keep
+// x * element size a multiple of 16 bytes and every coordinate >= 0.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// The issuing thread's bulk stores have finished reading shared memory (the
+// source may be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// The issuing thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(void *p, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 // ---- tcgen05 ----------------------------------------------------------------------
