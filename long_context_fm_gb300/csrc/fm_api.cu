@@ -31,8 +31,8 @@ fm_status fm_bwd_prepare(int d, bool precise);
 fm_status fm_fwd_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const CUtensorMap &to, const FwdArgs &a, int d, bool precise, cudaStream_t stream);
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const CUtensorMap &tdo, const BwdArgs &a, int d,
-                             bool precise, cudaStream_t stream);
+                             const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                             const BwdArgs &a, int d, bool precise, cudaStream_t stream);
 
 namespace {
 
@@ -88,16 +88,16 @@ bool make_tmap_u8(CUtensorMap *map, const void *base, int BH, int rows, int cols
     return r == CUDA_SUCCESS;
 }
 
-// O, fp32 or bf16 [BH, Nq, d], viewed as 3-D (d, Nq, BH) for TMA stores: box =
-// 64 bytes (16 fp32 or 32 bf16 columns) x 32 rows, 64-byte swizzle; rows at
-// or beyond Nq are not written.
-bool make_tmap_out(CUtensorMap *map, void *base, int BH, int Nq, int d, bool f32)
+// An output (O, dK or dV), fp32 or bf16 [BH, rows, d], viewed as 3-D (d, rows,
+// BH) for TMA stores: box = 64 bytes (16 fp32 or 32 bf16 columns) x 32 rows,
+// 64-byte swizzle; rows at or beyond `rows` are not written.
+bool make_tmap_out(CUtensorMap *map, void *base, int BH, int rows, int d, bool f32)
 {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t esz = f32 ? 4 : 2;
-    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Nq, (cuuint64_t)BH};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * esz, (cuuint64_t)Nq * d * esz};
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * esz, (cuuint64_t)rows * d * esz};
     const cuuint32_t box[3] = {(cuuint32_t)(64 / esz), 32, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
@@ -398,10 +398,12 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < need) return FM_ERR_WORKSPACE;
     if (!plan || ((uintptr_t)plan & 255u)) return FM_ERR_INVALID_ARG;
     if ((st = check_device()) != FM_OK) return st;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     float *dq_acc = reinterpret_cast<float *>(ws);
     if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
-        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, 64))
+        !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, 64) ||
+        !make_tmap_out(&tdk, dk, B * H, N, d, grad_dtype == FM_DT_F32) ||
+        !make_tmap_out(&tdv, dv, B * H, N, d, grad_dtype == FM_DT_F32))
         return FM_ERR_CUDA;
     float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * Nq * d * 4));
     const int64_t rows = (int64_t)B * H * Nq;
@@ -423,7 +425,7 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     a.scale = scale; a.scale_log2 = scale * 1.4426950408889634f;
     a.g_f32 = grad_dtype == FM_DT_F32;
     wait_test_args(1, &a.wait_limit, &a.withhold);
-    if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
+    if ((st = fm_bwd_main_launch(tq, tk, tv, tdo, tdk, tdv, a, d, (flags & FM_FLAG_PRECISE) != 0, s)) != FM_OK)
         return st;
     return dq_direct ? FM_OK : fm_bwd_post_launch(dq_acc, dq, scale, rows * d, s);
 }

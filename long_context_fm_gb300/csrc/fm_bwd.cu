@@ -148,7 +148,8 @@ struct BwdSmem {
     static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
     static constexpr int kdS = kdO + kStages * kQTile;      // dS^T (high part)  [kdSBufs]
     static constexpr int kdSlo = kdS + kdSBufs * kOp;       // precise: dS^T low part
-    static constexpr int kUnit = PRECISE ? kdSlo + kOp : kdSlo;   // int [kBwdUnitRing][4]: unit ring
+    static constexpr int kOst = PRECISE ? kdSlo + kOp : kdSlo;    // dK / dV staging: [16 warps][32 rows][64 bytes]
+    static constexpr int kUnit = kOst + 16 * 2048;          // int [kBwdUnitRing][4]: unit ring
     static constexpr int kStat = kUnit + kBwdUnitRing * 16;  // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
     static constexpr int kNumBar = BB_COUNT;
@@ -172,6 +173,7 @@ template <int D, bool PRECISE>
 __global__ void __launch_bounds__(800, 1)
     fm_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                   const BwdArgs a)
 {
     using S = BwdSmem<D, PRECISE>;
@@ -644,17 +646,34 @@ __global__ void __launch_bounds__(800, 1)
             // ------------------------------------------------ dK, dV epilogue
             // Warpgroups 0, 1 store the two column halves of dK; 2, 3 of dV.  The
             // accumulators are released to the next unit's first dV / dK product
-            // once read; a unit without halves stores zeros.
+            // once read; a unit without halves stores zeros.  The values leave
+            // through shared memory and TMA stores: each warp stages its 32 rows x
+            // 64 bytes (16 fp32 or 32 bf16 columns) at a time in a buffer of its
+            // own with the 64-byte swizzle (16-byte chunk q of row x at chunk
+            // q ^ ((x >> 1) & 3)), and the copy engine writes whole row segments
+            // and drops rows at or beyond N.  A buffer is rewritten once the
+            // previous store has read it.
             if (!ok) break;
             if (u.n_it > 0 && !warp_wait(&bars[BB_ACC], nu & 1, abort, a.status, a.wait_limit)) break;
             tc_fence_after();
-            const bool row_in = j < N;
-            const int64_t row = (int64_t)u.bh * N + j;
             const bool is_dk = wg < 2;
             const uint32_t tsrc = is_dk ? tdK : tdV;
             const float mul = is_dk ? a.scale : 1.f;
-            void *dst = is_dk ? a.dk : a.dv;
+            const CUtensorMap *tout = is_dk ? &tdk : &tdv;
             const int cbase = (wg & 1) * (D / 2);
+            uint8_t *stg = smem + S::kOst + (warp - 2) * 2048;
+            auto stage_store = [&](const uint4 (&pk)[4], int x) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), pk[q]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(tout, stg, x, kb + quarter * 32, u.bh);
+                    bulk_commit();
+                }
+            };
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 const int col = cbase + cc * 32;
@@ -667,21 +686,27 @@ __global__ void __launch_bounds__(800, 1)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) v[q] = 0u;
                 }
-                if (!row_in) continue;
                 if (a.g_f32) {
-                    float4 *pp = reinterpret_cast<float4 *>(reinterpret_cast<float *>(dst) + row * D + col);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        pp[q] = make_float4(__uint_as_float(v[4 * q]) * mul, __uint_as_float(v[4 * q + 1]) * mul,
-                                            __uint_as_float(v[4 * q + 2]) * mul, __uint_as_float(v[4 * q + 3]) * mul);
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 pk[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            pk[q] = make_uint4(__float_as_uint(__uint_as_float(v[16 * h + 4 * q]) * mul),
+                                               __float_as_uint(__uint_as_float(v[16 * h + 4 * q + 1]) * mul),
+                                               __float_as_uint(__uint_as_float(v[16 * h + 4 * q + 2]) * mul),
+                                               __float_as_uint(__uint_as_float(v[16 * h + 4 * q + 3]) * mul));
+                        stage_store(pk, col + 16 * h);
+                    }
                 } else {
-                    uint4 *pp = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(dst) + row * D + col);
+                    uint4 pk[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        pp[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                        pk[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
                                            pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
                                            pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
                                            pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
+                    stage_store(pk, col);
                 }
             }
             if (u.n_it > 0) {
@@ -690,6 +715,8 @@ __global__ void __launch_bounds__(800, 1)
                 ++nu;
             }
             }
+            // Every TMA store of dK / dV has completed before the CTA leaves.
+            if (lane == 0) bulk_wait_all();
         } else if (warp < 22) {
             // ------------------------------------------------ dQ drain
             // Thread = head-dim index (TMEM lane of dQ^T).  The half's 64 x d
@@ -804,8 +831,8 @@ static bool bwd_smem_ready()
 
 template <int D, bool PRECISE>
 static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                            const CUtensorMap &tdo, const BwdArgs &a,
-                            cudaStream_t stream)
+                            const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                            const BwdArgs &a, cudaStream_t stream)
 {
     constexpr int smem = BwdSmem<D, PRECISE>::kBytes;
     if (!bwd_smem_ready<D, PRECISE>()) return FM_ERR_CUDA;
@@ -819,7 +846,7 @@ static fm_status launch_bwd(const CUtensorMap &tq, const CUtensorMap &tk, const 
     BwdArgs args = a;
     args.sched_slot = (int)(next_slot.fetch_add(1, std::memory_order_relaxed) % kBwdSchedSlots);
     ProfScope ps(kKBwd, stream);
-    fm_bwd_kernel<D, PRECISE><<<grid, 800, smem, stream>>>(tq, tk, tv, tdo, args);
+    fm_bwd_kernel<D, PRECISE><<<grid, 800, smem, stream>>>(tq, tk, tv, tdo, tdk, tdv, args);
     return cudaPeekAtLastError() == cudaSuccess ? FM_OK : FM_ERR_CUDA;
 }
 
@@ -832,14 +859,14 @@ fm_status fm_bwd_prepare(int d, bool precise)
 }
 
 fm_status fm_bwd_main_launch(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const CUtensorMap &tdo, const BwdArgs &a, int d,
-                             bool precise, cudaStream_t stream)
+                             const CUtensorMap &tdo, const CUtensorMap &tdk, const CUtensorMap &tdv,
+                             const BwdArgs &a, int d, bool precise, cudaStream_t stream)
 {
     if (d == 128)
-        return precise ? launch_bwd<128, true>(tq, tk, tv, tdo, a, stream)
-                       : launch_bwd<128, false>(tq, tk, tv, tdo, a, stream);
-    return precise ? launch_bwd<64, true>(tq, tk, tv, tdo, a, stream)
-                   : launch_bwd<64, false>(tq, tk, tv, tdo, a, stream);
+        return precise ? launch_bwd<128, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)
+                       : launch_bwd<128, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
+    return precise ? launch_bwd<64, true>(tq, tk, tv, tdo, tdk, tdv, a, stream)
+                   : launch_bwd<64, false>(tq, tk, tv, tdo, tdk, tdv, a, stream);
 }
 
 fm_status fm_bwd_post_launch(const float *dq_acc, void *dq, float scale, int64_t n, cudaStream_t stream)
