@@ -61,7 +61,8 @@ enum {
     FB_KF0, FB_KF1, FB_KF2, FB_KE0, FB_KE1, FB_KE2,   // K stage loaded / released
     FB_VF0, FB_VF1, FB_VE0, FB_VE1,                   // V stage loaded / released
     FB_S0, FB_S1, FB_S2,                              // scores of buffer b computed
-    FB_P0, FB_P1, FB_P2,                              // P of buffer b written (both warpgroups)
+    FB_P0, FB_P1, FB_P2,                              // P of buffer b written, first 64 keys
+    FB_PB0, FB_PB1, FB_PB2,                           // P of buffer b written, last 64 keys
     FB_O0, FB_O1, FB_O2,                              // O += P V of a tile using buffer b completed
     FB_QE,                                            // the last scores of a unit have read Q
     FB_OE,                                            // the epilogue of a unit has read O
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int s = 0; s < kSB; ++s) {
                 mbar_init(&bars[FB_S0 + s], 1);
                 mbar_init(&bars[FB_P0 + s], 128);   // the tile's softmax warpgroup
+                mbar_init(&bars[FB_PB0 + s], 128);
                 mbar_init(&bars[FB_O0 + s], 1);
             }
             for (int s = 0; s < kUnitRing; ++s) {
@@ -449,21 +451,34 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         tc_fence_after();
                         const uint32_t tP = tmem + (g % kSB) * 128;
-                        if (FP8) {
-                            // B = V^T, K-major (d rows of 128 key bytes); A = P, 4 e4m3 per column
-                            const uint64_t dVt = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), 16, 1024);
+                        // The product in two halves over the keys: the first 64 as soon
+                        // as their P is written, the rest once all of P is (the softmax
+                        // releases the halves separately), so half of P V overlaps the
+                        // second half's exponentials.
+                        auto pv_half = [&](int h) {
+                            if (FP8) {
+                                // B = V^T, K-major (d rows of 128 key bytes); A = P, 4 e4m3 per column
+                                const uint64_t dVt = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), 16, 1024);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_ts_e4m3(tO, tP + kk * 8, sdesc_add(dVt, kk * 32), idesc_e4m3(128, D), (t > 0 || kk > 0));
-                        } else {
-                            const uint64_t dV = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), S::kBox, 1024);
+                                for (int kk = 2 * h; kk < 2 * h + 2; ++kk)
+                                    mma_ts_e4m3(tO, tP + kk * 8, sdesc_add(dVt, kk * 32), idesc_e4m3(128, D), (t > 0 || kk > 0));
+                            } else {
+                                const uint64_t dV = sdesc_sw128(smem_u32(smem + S::kV + vs * S::kTile), S::kBox, 1024);
 #pragma unroll
-                            for (int part = 0; part < NPART; ++part)   // P_hi V (+ P_lo V)
+                                for (int part = 0; part < NPART; ++part)   // P_hi V (+ P_lo V)
 #pragma unroll
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_ts(tO, tP + part * 64 + kk * 8, sdesc_add(dV, kk * 2048), idO,
-                                           (t > 0 || part > 0 || kk > 0));
+                                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                                        mma_ts(tO, tP + part * 64 + kk * 8, sdesc_add(dV, kk * 2048), idO,
+                                               (t > 0 || part > 0 || kk > 0));
+                            }
+                        };
+                        pv_half(0);
+                        if (!mbar_wait(&bars[FB_PB0 + g % kSB], (g / kSB) & 1, abort, a.status, a.wait_limit)) {
+                            run = false;
+                            break;
                         }
+                        tc_fence_after();
+                        pv_half(1);
                         tc_commit(&bars[FB_O0 + g % kSB]);
                         tc_commit(&bars[FB_VE0 + vs]);
                     }
@@ -682,15 +697,22 @@ __global__ void __launch_bounds__(384, 1)
                         }
                         if (!FP8) tmem_st16(tS + lane_off + hh * 16, hi);
                         if (PRECISE) tmem_st16(tS + lane_off + 64 + hh * 16, lo);
+                        if (hh == 1) {
+                            // The first 64 keys' P is complete: release it to P V.
+                            if (FP8) tmem_st16(tS + lane_off, reinterpret_cast<const uint32_t (&)[16]>(f8[0]));
+                            tmem_st_wait();
+                            tc_fence_before();
+                            mbar_arrive(&bars[FB_P0 + bb]);
+                        }
                     }
-                    if (FP8) tmem_st32(tS + lane_off, f8);
+                    if (FP8) tmem_st16(tS + lane_off + 16, reinterpret_cast<const uint32_t (&)[16]>(f8[16]));
                     float s0, s1;
                     f2_unpack(sum2, s0, s1);
                     l = (m == m_new ? l : l * ex2(m - m_new)) + (s0 + s1);
                     m = m_new;
                     tmem_st_wait();
                     tc_fence_before();
-                    mbar_arrive(&bars[FB_P0 + bb]);
+                    mbar_arrive(&bars[FB_PB0 + bb]);
                     // The mask of this warpgroup's next tile, while it waits for its scores.
                     if (next_pred) build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
                 }
