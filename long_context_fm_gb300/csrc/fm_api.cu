@@ -88,9 +88,9 @@ bool make_tmap_u8(CUtensorMap *map, const void *base, int BH, int rows, int cols
     return r == CUDA_SUCCESS;
 }
 
-// An output (O, dK or dV), fp32 or bf16 [BH, rows, d], viewed as 3-D (d, rows,
-// BH) for TMA stores: box = 64 bytes (16 fp32 or 32 bf16 columns) x 32 rows,
-// 64-byte swizzle; rows at or beyond `rows` are not written.
+// O, fp32 or bf16 [BH, rows, d], viewed as 3-D (d, rows, BH) for TMA stores:
+// box = 64 bytes (16 fp32 or 32 bf16 columns) x 32 rows, 64-byte swizzle; rows
+// at or beyond `rows` are not written.
 bool make_tmap_out(CUtensorMap *map, void *base, int BH, int rows, int d, bool f32)
 {
     auto fn = encode_fn();
@@ -102,6 +102,26 @@ bool make_tmap_out(CUtensorMap *map, void *base, int BH, int rows, int d, bool f
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// dK or dV, fp32 or bf16 [BH, rows, d], viewed as 3-D (d, rows, BH) for TMA
+// stores of 32 columns x 32 rows: fp32 boxes of 128-byte rows with the
+// 128-byte swizzle, bf16 boxes of 64-byte rows with the 64-byte swizzle; rows
+// at or beyond `rows` are not written.
+bool make_tmap_grad(CUtensorMap *map, void *base, int BH, int rows, int d, bool f32)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t esz = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)BH};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * esz, (cuuint64_t)rows * d * esz};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -402,8 +422,8 @@ fm_status fm_attn_bwd_rows(const void *q, const void *k, const void *v, const vo
     float *dq_acc = reinterpret_cast<float *>(ws);
     if (!make_tmap_bf16(&tq, q, B * H, Nq, d, 64) || !make_tmap_bf16(&tk, k, B * H, N, d, 128) ||
         !make_tmap_bf16(&tv, v, B * H, N, d, 128) || !make_tmap_bf16(&tdo, dO, B * H, Nq, d, 64) ||
-        !make_tmap_out(&tdk, dk, B * H, N, d, grad_dtype == FM_DT_F32) ||
-        !make_tmap_out(&tdv, dv, B * H, N, d, grad_dtype == FM_DT_F32))
+        !make_tmap_grad(&tdk, dk, B * H, N, d, grad_dtype == FM_DT_F32) ||
+        !make_tmap_grad(&tdv, dv, B * H, N, d, grad_dtype == FM_DT_F32))
         return FM_ERR_CUDA;
     float *Dvec = reinterpret_cast<float *>((uint8_t *)ws + align256((int64_t)B * H * Nq * d * 4));
     const int64_t rows = (int64_t)B * H * Nq;

@@ -116,6 +116,7 @@ enum {
     BB_PE0, BB_PE1, BB_DSE0, BB_DSE1, BB_DQF0, BB_DQF1, BB_DQE0, BB_DQE1, BB_ACC, BB_DRAIN0, BB_DRAIN1, BB_SFD0, BB_SFD1,
     BB_KVE,                                   // the unit's S^T, dP^T and dQ^T have read K and V
     BB_ACCE,                                  // the unit's epilogue has read dK and dV
+    BB_STG,                                   // every P/dS warp's dK / dV stores have read their staging
     BB_UF0, BB_UF1, BB_UF2, BB_UF3,           // unit ring: claimed unit written
     BB_UE0, BB_UE1, BB_UE2, BB_UE3,           // unit ring: every reader has read it
     BB_COUNT
@@ -148,7 +149,10 @@ struct BwdSmem {
     static constexpr int kdO = kQ + kStages * kQTile;       // [kStages]
     static constexpr int kdS = kdO + kStages * kQTile;      // dS^T (high part)  [kdSBufs]
     static constexpr int kdSlo = kdS + kdSBufs * kOp;       // precise: dS^T low part
-    static constexpr int kOst = PRECISE ? kdSlo + kOp : kdSlo;    // dK / dV staging: [16 warps][32 rows][64 bytes]
+    // dK / dV staging: the dS^T tiles and these 32 KB after them (64 KB,
+    // contiguous in both modes): [16 warps][32 rows][128 bytes].
+    static constexpr int kOst = PRECISE ? kdSlo + kOp : kdSlo;
+    static_assert(kOst == kdS + 32768, "the staging of the dK / dV stores follows the dS^T tiles");
     static constexpr int kUnit = kOst + 16 * 2048;          // int [kBwdUnitRing][4]: unit ring
     static constexpr int kStat = kUnit + kBwdUnitRing * 16;  // -lse*log2e [kStages][64], D [kStages][64]
     static constexpr int kBar = kStat + 2 * kStages * 64 * 4;
@@ -234,6 +238,7 @@ __global__ void __launch_bounds__(800, 1)
             mbar_init(&bars[BB_ACC], 1);
             mbar_init(&bars[BB_KVE], 3);      // S^T, dP^T and dQ^T issuers, after a unit's last product
             mbar_init(&bars[BB_ACCE], 512);   // P/dS threads, after the unit's dK, dV epilogue
+            mbar_init(&bars[BB_STG], 16);     // lane 0 of each P/dS warp, after its stores read the staging
             for (int s2 = 0; s2 < kBwdUnitRing; ++s2) {
                 mbar_init(&bars[BB_UF0 + s2], 1);
                 mbar_init(&bars[BB_UE0 + s2], kBwdUnitReaders);
@@ -535,6 +540,7 @@ __global__ void __launch_bounds__(800, 1)
             const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
             int G = 0;      // halves begun (CTA-wide)
             int nu = 0;     // units with halves finished
+            int nstg = 0;   // epilogues finished (phases of BB_STG)
             bool ok = true;
             Unit u;
             for (int k = 0; ok; ++k) {
@@ -647,33 +653,30 @@ __global__ void __launch_bounds__(800, 1)
             // Warpgroups 0, 1 store the two column halves of dK; 2, 3 of dV.  The
             // accumulators are released to the next unit's first dV / dK product
             // once read; a unit without halves stores zeros.  The values leave
-            // through shared memory and TMA stores: each warp stages its 32 rows x
-            // 64 bytes (16 fp32 or 32 bf16 columns) at a time in a buffer of its
-            // own with the 64-byte swizzle (16-byte chunk q of row x at chunk
-            // q ^ ((x >> 1) & 3)), and the copy engine writes whole row segments
-            // and drops rows at or beyond N.  A buffer is rewritten once the
-            // previous store has read it.
+            // through shared memory and TMA stores of 32 columns x 32 rows (fp32:
+            // 128-byte rows, 128-byte swizzle, 16-byte chunk q of row x at chunk
+            // q ^ (x & 7); bf16: 64-byte rows, 64-byte swizzle, chunk q at
+            // q ^ ((x >> 1) & 3)); the copy engine writes whole row segments and
+            // drops rows at or beyond N.  Staging: 4 KB per warp in the dS^T tiles
+            // and the 32 KB after them, free once the dK and dQ^T products of the
+            // unit's last halves have read dS^T; the next unit's dS^T is written
+            // once every warp's stores have read their staging (BB_STG).
             if (!ok) break;
             if (u.n_it > 0 && !warp_wait(&bars[BB_ACC], nu & 1, abort, a.status, a.wait_limit)) break;
+            {
+                const int back = S::kdSBufs;
+                bool dse_ok = true;
+                for (int h = (G > back ? G - back : 0); h < G && dse_ok; ++h)
+                    dse_ok = warp_wait(&bars[BB_DSE0 + (h % back)], (h / back) & 1, abort, a.status, a.wait_limit);
+                if (!dse_ok) break;
+            }
             tc_fence_after();
             const bool is_dk = wg < 2;
             const uint32_t tsrc = is_dk ? tdK : tdV;
             const float mul = is_dk ? a.scale : 1.f;
             const CUtensorMap *tout = is_dk ? &tdk : &tdv;
             const int cbase = (wg & 1) * (D / 2);
-            uint8_t *stg = smem + S::kOst + (warp - 2) * 2048;
-            auto stage_store = [&](const uint4 (&pk)[4], int x) {
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), pk[q]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_3d(tout, stg, x, kb + quarter * 32, u.bh);
-                    bulk_commit();
-                }
-            };
+            uint8_t *stg = sdS + (warp - 2) * 4096;
 #pragma unroll
             for (int cc = 0; cc < D / 64; ++cc) {
                 const int col = cbase + cc * 32;
@@ -686,27 +689,32 @@ __global__ void __launch_bounds__(800, 1)
 #pragma unroll
                     for (int q = 0; q < 32; ++q) v[q] = 0u;
                 }
+                if (cc > 0) {              // the previous store has read the buffer
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                }
                 if (a.g_f32) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 pk[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            pk[q] = make_uint4(__float_as_uint(__uint_as_float(v[16 * h + 4 * q]) * mul),
-                                               __float_as_uint(__uint_as_float(v[16 * h + 4 * q + 1]) * mul),
-                                               __float_as_uint(__uint_as_float(v[16 * h + 4 * q + 2]) * mul),
-                                               __float_as_uint(__uint_as_float(v[16 * h + 4 * q + 3]) * mul));
-                        stage_store(pk, col + 16 * h);
-                    }
+                    for (int q = 0; q < 8; ++q)
+                        st_shared_v4(stg + lane * 128 + ((q ^ (lane & 7)) << 4),
+                                     make_uint4(__float_as_uint(__uint_as_float(v[4 * q]) * mul),
+                                                __float_as_uint(__uint_as_float(v[4 * q + 1]) * mul),
+                                                __float_as_uint(__uint_as_float(v[4 * q + 2]) * mul),
+                                                __float_as_uint(__uint_as_float(v[4 * q + 3]) * mul)));
                 } else {
-                    uint4 pk[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        pk[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
-                                           pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
-                                           pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
-                                           pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul));
-                    stage_store(pk, col);
+                        st_shared_v4(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4),
+                                     make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * mul, __uint_as_float(v[8 * q + 1]) * mul),
+                                                pack_bf16x2(__uint_as_float(v[8 * q + 2]) * mul, __uint_as_float(v[8 * q + 3]) * mul),
+                                                pack_bf16x2(__uint_as_float(v[8 * q + 4]) * mul, __uint_as_float(v[8 * q + 5]) * mul),
+                                                pack_bf16x2(__uint_as_float(v[8 * q + 6]) * mul, __uint_as_float(v[8 * q + 7]) * mul)));
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(tout, stg, col, kb + quarter * 32, u.bh);
+                    bulk_commit();
                 }
             }
             if (u.n_it > 0) {
@@ -714,6 +722,14 @@ __global__ void __launch_bounds__(800, 1)
                 mbar_arrive(&bars[BB_ACCE]);
                 ++nu;
             }
+            // The staging (with the dS^T tiles) is free once every warp's stores
+            // have read it; each warp waits for all sixteen, so the phases of
+            // BB_STG stay in step with the units.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[BB_STG]);
+            if (!warp_wait(&bars[BB_STG], nstg & 1, abort, a.status, a.wait_limit)) break;
+            ++nstg;
             }
             // Every TMA store of dK / dV has completed before the CTA leaves.
             if (lane == 0) bulk_wait_all();
