@@ -57,7 +57,8 @@ typedef enum {
     FM_ERR_PLAN_MISMATCH = 5,    /* plan built for other shapes or tile sizes            */
     FM_ERR_WORKSPACE = 6,        /* workspace missing or too small                       */
     FM_ERR_CUDA = 7,             /* a CUDA runtime / driver call failed                  */
-    FM_ERR_TIMEOUT = 8           /* a bounded device-side wait ran out (kernel returned) */
+    FM_ERR_TIMEOUT = 8,          /* a bounded device-side wait ran out (kernel returned) */
+    FM_ERR_DEBUG_CHECK = 9       /* a device-side check of an FM_DEBUG build failed      */
 } fm_status;
 
 enum { FM_TILE_SKIP = 0, FM_TILE_FULL = 1, FM_TILE_PARTIAL = 2 };

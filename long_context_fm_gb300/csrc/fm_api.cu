@@ -262,6 +262,7 @@ const char *fm_status_string(fm_status st)
     case FM_ERR_WORKSPACE: return "workspace missing or too small";
     case FM_ERR_CUDA: return "CUDA error";
     case FM_ERR_TIMEOUT: return "device-side wait timed out";
+    case FM_ERR_DEBUG_CHECK: return "device-side check of a debug build failed";
     }
     return "unknown status";
 }

@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(800, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
     int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
+    volatile int *dbg = reinterpret_cast<volatile int *>(smem + S::kMisc + 16);   // debug counters [3]
 
     const int warp = warp_id(), lane = lane_id();
     const PlanLayout &L = a.L;
@@ -256,6 +257,7 @@ __global__ void __launch_bounds__(800, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    if (kDebugChecks && threadIdx.x == 0 && (tmem & 0xffffu) != 0u) set_status(a.status, FM_ERR_DEBUG_CHECK);
     // TMEM: dK, dV, then two score buffers b = half & 1: S^T at 256 + 128 b
     // (then P^T), dP^T at 320 + 128 b (then dQ^T, once dS^T has been written).
     const uint32_t tdK = tmem, tdV = tmem + 128, tS0 = tmem + 256, tdP0 = tmem + 320;
@@ -334,7 +336,8 @@ __global__ void __launch_bounds__(800, 1)
             const int withheld = (a.withhold && blockIdx.x == 0) ? 1 : -1;
             bool run = true;
             Unit u;
-            for (int k = 0; run; ++k) {
+            int k = 0;      // ring entries published (claims, the terminating one included)
+            for (; run; ++k) {
                 // Claim the next unit into ring entry k once every reader is done
                 // with the entry's previous unit.
                 const int slot = k % kBwdUnitRing;
@@ -354,6 +357,11 @@ __global__ void __launch_bounds__(800, 1)
                     mbar_arrive(&bars[BB_UF0 + slot]);
                 }
                 if (!valid) break;
+                if (kDebugChecks && (u.n_it < 0 || u.n_it > 2 * L.n_q)) {
+                    if (lane == 0) set_status(a.status, FM_ERR_DEBUG_CHECK);
+                    *abort = 1;
+                    break;
+                }
                 if (u.n_it == 0) continue;
                 if (nkv > 0 && !warp_wait(&bars[BB_KVE], (nkv - 1) & 1, abort, a.status, a.wait_limit)) break;
                 if (lane == 0) {
@@ -366,6 +374,16 @@ __global__ void __launch_bounds__(800, 1)
                 }
                 ++nkv;
                 for (int it = 0; it < u.n_it; ++it, ++G) {
+                    if (kDebugChecks && (it & 1) == 0) {   // a Q tile of the column and a FULL or PARTIAL label
+                        const int e = u.list[it >> 1];
+                        const int lab = (int)((unsigned)e >> kLabelShift);
+                        if ((e & kTileMask) >= L.n_q || (lab != FM_TILE_FULL && lab != FM_TILE_PARTIAL)) {
+                            if (lane == 0) set_status(a.status, FM_ERR_DEBUG_CHECK);
+                            *abort = 1;
+                            run = false;
+                            break;
+                        }
+                    }
                     const int q0 = q0_of(u, it);
                     const int st = G % NST;
                     // lse and D of the half's rows, loaded before the stage wait so
@@ -402,6 +420,11 @@ __global__ void __launch_bounds__(800, 1)
                     }
                     mbar_arrive(&bars[BB_QF0 + st]);     // 32 arrivals after the stores (+1 expect_tx)
                 }
+            }
+            if (kDebugChecks && lane == 0) {
+                dbg[0] = G;
+                dbg[1] = nkv;
+                dbg[2] = k + 1;
             }
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
@@ -792,6 +815,32 @@ __global__ void __launch_bounds__(800, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // Debug build: every pipeline barrier has completed as many phases as the
+    // CTA's halves (G), units with halves, units and ring entries imply.
+    if (kDebugChecks && threadIdx.x == 0 && *ok_sh && !*abort) {
+        const int G = dbg[0], NU = dbg[1], NK = dbg[2];
+        auto cnt = [](int total, int period, int idx) { return total > idx ? (total - 1 - idx) / period + 1 : 0; };
+        bool good = mbar_phase_count_ok(&bars[BB_KV], NU) && mbar_phase_count_ok(&bars[BB_KVE], NU) &&
+                    mbar_phase_count_ok(&bars[BB_ACC], NU) && mbar_phase_count_ok(&bars[BB_ACCE], NU) &&
+                    mbar_phase_count_ok(&bars[BB_STG], NK - 1) && mbar_phase_count_ok(&bars[BB_DRAIN0], 1) &&
+                    mbar_phase_count_ok(&bars[BB_DRAIN1], 0);
+        for (int s2 = 0; s2 < NST; ++s2)
+            good = good && mbar_phase_count_ok(&bars[BB_QF0 + s2], cnt(G, NST, s2)) &&
+                   mbar_phase_count_ok(&bars[BB_QE0 + s2], cnt(G, NST, s2));
+        for (int b = 0; b < 2; ++b) {
+            const int c = cnt(G, 2, b);
+            good = good && mbar_phase_count_ok(&bars[BB_SF0 + b], c) && mbar_phase_count_ok(&bars[BB_SFD0 + b], c) &&
+                   mbar_phase_count_ok(&bars[BB_PF0 + b], c) && mbar_phase_count_ok(&bars[BB_PE0 + b], c) &&
+                   mbar_phase_count_ok(&bars[BB_DF0 + b], c) && mbar_phase_count_ok(&bars[BB_DQF0 + b], c) &&
+                   mbar_phase_count_ok(&bars[BB_DQE0 + b], c);
+        }
+        for (int b = 0; b < S::kdSBufs; ++b)
+            good = good && mbar_phase_count_ok(&bars[BB_DSE0 + b], cnt(G, S::kdSBufs, b));
+        for (int s2 = 0; s2 < kBwdUnitRing; ++s2)
+            good = good && mbar_phase_count_ok(&bars[BB_UF0 + s2], cnt(NK, kBwdUnitRing, s2)) &&
+                   mbar_phase_count_ok(&bars[BB_UE0 + s2], cnt(NK, kBwdUnitRing, s2));
+        if (!good) set_status(a.status, FM_ERR_DEBUG_CHECK);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);

@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + S::kMisc);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + S::kMisc + 4);
     int *ok_sh = reinterpret_cast<int *>(smem + S::kMisc + 12);
+    volatile int *dbg = reinterpret_cast<volatile int *>(smem + S::kMisc + 16);   // debug counters [3]
     volatile int *sUnit = reinterpret_cast<volatile int *>(smem + S::kUnit);   // [kUnitRing][4]
     volatile int *sFlag = reinterpret_cast<volatile int *>(smem + S::kFlag);
 
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(384, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    if (kDebugChecks && threadIdx.x == 0 && (tmem & 0xffffu) != 0u) set_status(a.status, FM_ERR_DEBUG_CHECK);
 
     // Persistent CTAs with dynamic scheduling: the K producer of each CTA claims
     // the next work unit (b, h, 128-row Q tile) of the plan's longest-first order
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(384, 1)
             const int withheld = (a.withhold && blockIdx.x == 0) ? 1 : -1;
             bool run = true;
             Unit u;
-            for (int k = 0; run; ++k) {
+            int k = 0;    // ring entries published (claims, the terminating one included)
+            for (; run; ++k) {
                 // Claim the next unit into ring entry k once every reader is done
                 // with the entry's previous unit.
                 const int slot = k % kUnitRing;
@@ -303,6 +306,11 @@ __global__ void __launch_bounds__(384, 1)
                     mbar_arrive(&bars[FB_UF0 + slot]);
                 }
                 if (!valid) break;
+                if (kDebugChecks && (u.n < 0 || u.n > L.n_k)) {
+                    if (lane == 0) set_status(a.status, FM_ERR_DEBUG_CHECK);
+                    *abort = 1;
+                    break;
+                }
                 if (u.n == 0) continue;
                 if (nq > 0 && !warp_wait(&bars[FB_QE], (nq - 1) & 1, abort, a.status, a.wait_limit)) break;
                 if (lane == 0) {
@@ -314,6 +322,15 @@ __global__ void __launch_bounds__(384, 1)
                 ++nq;
                 int e_next = u.list[0];
                 for (int t = 0; t < u.n; ++t, ++g) {
+                    if (kDebugChecks) {   // a KV tile of the row and a FULL or PARTIAL label
+                        const int lab = (int)((unsigned)e_next >> kLabelShift);
+                        if ((e_next & kTileMask) >= L.n_k || (lab != FM_TILE_FULL && lab != FM_TILE_PARTIAL)) {
+                            if (lane == 0) set_status(a.status, FM_ERR_DEBUG_CHECK);
+                            *abort = 1;
+                            run = false;
+                            break;
+                        }
+                    }
                     const int kb = (e_next & kTileMask) * 128;
                     if (t + 1 < u.n) e_next = u.list[t + 1];
                     const int ks = g % KS;
@@ -329,6 +346,7 @@ __global__ void __launch_bounds__(384, 1)
                     }
                 }
             }
+            if (kDebugChecks && lane == 0) dbg[2] = k + 1;
             // Drain copies still in flight (only possible after an abort).
             if (lane == 0 && *abort) {
                 if (nq > 0) mbar_wait_drain(&bars[FB_Q], (nq - 1) & 1, a.status, a.wait_limit);
@@ -424,6 +442,10 @@ __global__ void __launch_bounds__(384, 1)
                 // Every MMA of this CTA (both issuers) completes before TMEM is released.
                 tc_commit(&bars[FB_DRAIN]);
                 mbar_wait_drain(&bars[FB_DRAIN], 0, a.status, a.wait_limit);
+                if (kDebugChecks) {
+                    dbg[0] = g;
+                    dbg[1] = nq;
+                }
             }
         } else if (warp == 11) {
             warp_regs_dec<kRegsIssue>();
@@ -812,6 +834,29 @@ __global__ void __launch_bounds__(384, 1)
     }
     tc_fence_before();
     __syncthreads();
+    // Debug build: every pipeline barrier has completed as many phases as the
+    // CTA's tiles (g), units with tiles and ring entries imply.
+    if (kDebugChecks && threadIdx.x == 0 && *ok_sh && !*abort) {
+        const int G = dbg[0], NU = dbg[1], NK = dbg[2];
+        auto cnt = [](int total, int period, int idx) { return total > idx ? (total - 1 - idx) / period + 1 : 0; };
+        bool good = mbar_phase_count_ok(&bars[FB_Q], NU) && mbar_phase_count_ok(&bars[FB_QE], NU) &&
+                    mbar_phase_count_ok(&bars[FB_OE], NU) && mbar_phase_count_ok(&bars[FB_DRAIN], 1);
+        for (int b = 0; b < kSB; ++b) {
+            const int c = cnt(G, kSB, b);
+            good = good && mbar_phase_count_ok(&bars[FB_S0 + b], c) && mbar_phase_count_ok(&bars[FB_P0 + b], c) &&
+                   mbar_phase_count_ok(&bars[FB_PB0 + b], c) && mbar_phase_count_ok(&bars[FB_O0 + b], c);
+        }
+        for (int s2 = 0; s2 < KS; ++s2)
+            good = good && mbar_phase_count_ok(&bars[FB_KF0 + s2], cnt(G, KS, s2)) &&
+                   mbar_phase_count_ok(&bars[FB_KE0 + s2], cnt(G, KS, s2));
+        for (int s2 = 0; s2 < VS; ++s2)
+            good = good && mbar_phase_count_ok(&bars[FB_VF0 + s2], cnt(G, VS, s2)) &&
+                   mbar_phase_count_ok(&bars[FB_VE0 + s2], cnt(G, VS, s2));
+        for (int s2 = 0; s2 < kUnitRing; ++s2)
+            good = good && mbar_phase_count_ok(&bars[FB_UF0 + s2], cnt(NK, kUnitRing, s2)) &&
+                   mbar_phase_count_ok(&bars[FB_UE0 + s2], cnt(NK, kUnitRing, s2));
+        if (!good) set_status(a.status, FM_ERR_DEBUG_CHECK);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);

@@ -187,6 +187,17 @@ enum KernelId {
 // Devices a process may use (per-device caches of kernel attributes).
 constexpr int kMaxDevices = 64;
 
+// Device-side checks of the FM_DEBUG build (a compile definition; the release
+// build compiles them out): plan entries within range, the TMEM allocation
+// at column 0, and at the end of each CTA every pipeline mbarrier's phase
+// parity against the number of tiles, halves and units the CTA processed.  A
+// failed check records FM_ERR_DEBUG_CHECK in the caller's status word.
+#ifdef FM_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
 // Default limit of every bounded device-side wait, in SM clock cycles
 // (about 1.5 s at 1.4-2.1 GHz): far above any legitimate wait inside a CTA.
 constexpr long long kWaitLimitCycles = 3000000000LL;

@@ -135,6 +135,13 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
     }
 }
 
+// An mbarrier that has completed `completed` phases is in phase `completed`:
+// the phase with that parity has not completed yet (checks the count mod 2).
+__device__ __forceinline__ bool mbar_phase_count_ok(uint64_t *bar, int completed)
+{
+    return !mbar_test_wait(bar, (uint32_t)completed & 1u);
+}
+
 // Warp-uniform wait: every lane waits (bounded); the warp proceeds only if
 // all lanes saw the phase complete, so .sync.aligned instructions that follow
 // are executed by the whole warp or by none of it.

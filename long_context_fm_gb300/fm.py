@@ -12,7 +12,9 @@ import os
 import numpy as np
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfm.so")
+# FM_LIBRARY selects another build of the same library (the FM_DEBUG build of
+# build.build(debug=True)); by default the in-tree release build.
+_LIB_PATH = os.environ.get("FM_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfm.so")
 if not os.path.exists(_LIB_PATH):
     raise ImportError(f"{_LIB_PATH} is missing: build it with "
                       "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
@@ -20,6 +22,7 @@ _lib = ctypes.CDLL(_LIB_PATH)
 
 FM_OK, FM_ERR_INVALID_ARG, FM_ERR_UNSUPPORTED, FM_ERR_UNREPRESENTABLE = 0, 1, 2, 3
 FM_ERR_BAD_BOUNDS, FM_ERR_PLAN_MISMATCH, FM_ERR_WORKSPACE, FM_ERR_CUDA, FM_ERR_TIMEOUT = 4, 5, 6, 7, 8
+FM_ERR_DEBUG_CHECK = 9
 FM_TILE_SKIP, FM_TILE_FULL, FM_TILE_PARTIAL = 0, 1, 2
 FM_DT_BF16, FM_DT_F32 = 0, 1
 FM_FLAG_PRECISE = 1

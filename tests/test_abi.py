@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(fm):
 
 def test_abi_version_and_status_strings(fm):
     assert fm.fm_abi_version() == 6
-    for code in range(9):
+    for code in range(10):
         assert fm.fm_status_string(code) and "unknown" not in fm.fm_status_string(code)
     assert "unknown" in fm.fm_status_string(99)
 
