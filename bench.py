@@ -48,7 +48,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel, the hash of the source it was taken on (stale entries are ignored)
 # and the workload.
 NCU_TRAFFIC = {
-    ("bwd", "90c9125e660b4df5", "long_packing_128k"): 1649.414e6 + 1567.052e6,
+    ("bwd", "63f8834e03518abe", "long_packing_128k"): 1649.403e6 + 1566.780e6,
 }
 
 

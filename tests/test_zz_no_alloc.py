@@ -6,8 +6,8 @@ after start-up, plugins that are handed only their input and output
 buffers.  fm_attn_bwd_noalloc serves them by taking the backward's
 workspace from an array built into the library.  These tests call it
 through the C ABI and check that two calls in a row give the gradients of
-fm_attn_bwd (with a caller workspace) within the parity tolerance, and that
-a size beyond the built-in array is refused.  The file is collected last so
+fm_attn_bwd (with a caller workspace) and of the oracle within the parity
+tolerance, and that a size beyond the built-in array is refused.  The file is collected last so
 that a run stopping at the first failure has run everything else first; it
 also passes on its own in a fresh process.
 """
@@ -16,6 +16,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from long_context_fm_gb300 import workloads as W
 from parity import check_close
 
@@ -34,7 +35,9 @@ def fm():
 def test_noalloc_matches_workspace_backward_twice(fm, name, g_dtype):
     wl = W.SMALL[name]
     m = W.make_mask(wl)
-    q, k, v, dO = (t.cuda() for t in W.make_inputs(wl))
+    inputs = W.make_inputs(wl)
+    g_ref = oracle.backward(*inputs, m, wl.scale)
+    q, k, v, dO = (t.cuda() for t in inputs)
     att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"])
     o, lse = att.forward(q, k, v, wl.scale, o_dtype=torch.float32)
     ws = torch.empty(fm.fm_bwd_workspace_bytes(*q.shape), dtype=torch.uint8, device="cuda")
@@ -46,8 +49,9 @@ def test_noalloc_matches_workspace_backward_twice(fm, name, g_dtype):
         fm.fm_attn_bwd_noalloc(q, k, v, o, lse, dO, att.bounds, att.plan, wl.scale, *got, att.status)
         torch.cuda.synchronize()
         att.check_status()
-        for label, a, b in zip(("dQ", "dK", "dV"), got, ref):
+        for label, key, a, b in zip(("dQ", "dK", "dV"), ("dq", "dk", "dv"), got, ref):
             check_close(f"{label} call {call}", a.float().cpu().numpy(), b.float().cpu().numpy())
+            check_close(f"{label} call {call} vs oracle", a.float().cpu().numpy(), g_ref[key])
 
 
 def test_noalloc_refuses_sizes_beyond_the_builtin_array(fm):
