@@ -95,20 +95,14 @@ struct FwdSmem {
 };
 
 
-// Bits x of a 32-row group with lo <= x < hi (bounds clamped to [0, 32]).
+// Bits x of a 32-row group with lo <= x < hi (bounds clamped to [0, 32]): the
+// bits at or above lo and below hi, as two clamping funnel shifts (a shift by
+// 32 gives 0); empty when hi <= lo.
 __device__ __forceinline__ uint32_t row_bits32(int lo, int hi)
 {
     lo = min(max(lo, 0), 32);
     hi = min(max(hi, 0), 32);
-    if (hi <= lo) return 0u;
-    return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
-}
-
-// fp32 bits x, or -inf where bit (31 - sh) of `word` is set.
-__device__ __forceinline__ uint32_t neg_inf_where(uint32_t x, uint32_t word, uint32_t sh)
-{
-    const uint32_t m = (uint32_t)((int32_t)(word << sh) >> 31);
-    return (x & ~m) | (0xff800000u & m);
+    return __funnelshift_lc(0u, 0xffffffffu, (uint32_t)lo) & __funnelshift_rc(0xffffffffu, 0u, (uint32_t)(32 - hi));
 }
 
 constexpr int kSB = 3;              // score buffers in TMEM
@@ -548,6 +542,7 @@ __global__ void __launch_bounds__(384, 1)
             int g = 0;     // tiles begun (CTA-wide, both warpgroups)
             int nu = 0;    // units with tiles finished
             int nbf = 0;   // this warpgroup's partial tiles (their masks alternate between two buffers)
+            int mflag = 0; // build_mask's summary of the mask built last (read by the tile it is for)
             uint32_t *sMaskW = sMask + (warp - 2) * 256;   // this warp's two mask buffers
             // The mask of a partial tile as bits over this warp's 32 rows of the Q
             // tile (mask rows r0 + 32 quarter + x): word c has bit x set when that
@@ -558,19 +553,31 @@ __global__ void __launch_bounds__(384, 1)
             // warpgroup's previous tile) and turned into bits after that tile's P
             // is released (build_mask).
             int4 bnd[4];
+            // Four 16-byte loads (one per bound array) when the arrays allow it.
+            const bool vec_ok = (N & 3) == 0 && ((reinterpret_cast<uintptr_t>(a.lts) | reinterpret_cast<uintptr_t>(a.lte) |
+                                                  reinterpret_cast<uintptr_t>(a.uts) | reinterpret_cast<uintptr_t>(a.ute)) & 15u) == 0;
             auto load_bounds = [&](int e, const Unit &uu) {
                 const int kb = (e & kTileMask) * 128;
+                const int j0 = kb + lane * 4;
+                const int64_t o0 = (int64_t)uu.sidx * N + j0;
+                if (vec_ok && j0 + 4 <= N) {
+                    const int4 x = *reinterpret_cast<const int4 *>(a.lts + o0), y = *reinterpret_cast<const int4 *>(a.lte + o0);
+                    const int4 z = *reinterpret_cast<const int4 *>(a.uts + o0), u = *reinterpret_cast<const int4 *>(a.ute + o0);
+                    bnd[0] = make_int4(x.x, y.x, z.x, u.x);
+                    bnd[1] = make_int4(x.y, y.y, z.y, u.y);
+                    bnd[2] = make_int4(x.z, y.z, z.z, u.z);
+                    bnd[3] = make_int4(x.w, y.w, z.w, u.w);
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int j = kb + lane * 4 + c;
-                    bnd[c] = make_int4(0, 0, 0, 0);
-                    if (j < N) {
-                        const int64_t o = (int64_t)uu.sidx * N + j;
-                        bnd[c] = make_int4(a.lts[o], a.lte[o], a.uts[o], a.ute[o]);
+                    for (int c = 0; c < 4; ++c) {
+                        bnd[c] = make_int4(0, 0, 0, 0);
+                        if (j0 + c < N) bnd[c] = make_int4(a.lts[o0 + c], a.lte[o0 + c], a.uts[o0 + c], a.ute[o0 + c]);
                     }
                 }
             };
-            auto build_mask = [&](int e, const Unit &uu, uint32_t *dst) {
+            // Returns, for the whole warp, 0 when none of its rows is masked in the
+            // tile, 1 when all of them are masked in every column, else 2.
+            auto build_mask = [&](int e, const Unit &uu, uint32_t *dst) -> int {
                 const int kb = (e & kTileMask) * 128;
                 const int base = a.q_row0 + uu.qt * 128 + quarter * 32;
                 uint32_t wq[4];
@@ -582,7 +589,10 @@ __global__ void __launch_bounds__(384, 1)
                                 : 0xffffffffu;
                 }
                 *reinterpret_cast<uint4 *>(dst + lane * 4) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                const uint32_t any = __reduce_or_sync(0xffffffffu, wq[0] | wq[1] | wq[2] | wq[3]);
+                const uint32_t all = __reduce_and_sync(0xffffffffu, wq[0] & wq[1] & wq[2] & wq[3]);
                 __syncwarp();
+                return any == 0u ? 0 : (all == 0xffffffffu ? 1 : 2);
             };
             auto is_partial = [&](int e) {
                 return ((e >> kLabelShift) == FM_TILE_PARTIAL) || (e & kTileMask) * 128 + 128 > N;
@@ -607,7 +617,7 @@ __global__ void __launch_bounds__(384, 1)
                 int e_next = t0 < un.n ? un.list[t0] : 0;
                 if (live && t0 < un.n && is_partial(e_next)) {
                     load_bounds(e_next, un);
-                    build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
+                    mflag = build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
                 }
                 for (int t = t0; t < un.n; t += 2) {
                     const int gt = g0 + t;
@@ -631,16 +641,18 @@ __global__ void __launch_bounds__(384, 1)
                             tmem_ld32(tS + lane_off + c * 32, reinterpret_cast<uint32_t (&)[32]>(sv[c * 32]));
                         tmem_ld_wait();
                         tmem_reg_fence(sv);
-                        if (pred) {
-                            // The lane is the bit of its row; masked scores become -inf.
-                            const uint32_t sh = 31u - (uint32_t)lane;
+                        if (pred && mflag != 0) {
+                            // The lane is the bit of its row; masked scores become -inf
+                            // (every score when the whole warp is masked, mflag == 1).
+                            const uint32_t lb = 1u << lane;
+                            const uint32_t all = (mflag == 1) ? 0xffffffffu : 0u;
 #pragma unroll
                             for (int c4 = 0; c4 < 32; ++c4) {
                                 const uint4 mw = mk[c4];
-                                sv[4 * c4 + 0] = neg_inf_where(sv[4 * c4 + 0], mw.x, sh);
-                                sv[4 * c4 + 1] = neg_inf_where(sv[4 * c4 + 1], mw.y, sh);
-                                sv[4 * c4 + 2] = neg_inf_where(sv[4 * c4 + 2], mw.z, sh);
-                                sv[4 * c4 + 3] = neg_inf_where(sv[4 * c4 + 3], mw.w, sh);
+                                sv[4 * c4 + 0] = ((mw.x | all) & lb) ? 0xff800000u : sv[4 * c4 + 0];
+                                sv[4 * c4 + 1] = ((mw.y | all) & lb) ? 0xff800000u : sv[4 * c4 + 1];
+                                sv[4 * c4 + 2] = ((mw.z | all) & lb) ? 0xff800000u : sv[4 * c4 + 2];
+                                sv[4 * c4 + 3] = ((mw.w | all) & lb) ? 0xff800000u : sv[4 * c4 + 3];
                             }
                         }
                         float mx4[4] = {__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]),
@@ -736,7 +748,7 @@ __global__ void __launch_bounds__(384, 1)
                     tc_fence_before();
                     mbar_arrive(&bars[FB_PB0 + bb]);
                     // The mask of this warpgroup's next tile, while it waits for its scores.
-                    if (next_pred) build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
+                    if (next_pred) mflag = build_mask(e_next, un, sMaskW + (nbf & 1) * 128);
                 }
                 g = g0 + un.n;
                 // ------------------------------------------------ epilogue
