@@ -10,8 +10,10 @@ in HBM.  `e2e` repeats the step through the C ABI from pinned host buffers:
 row-form mask conversion on the host, host-to-device copies of Q, K, V, dO
 and the bounds, the device work, and device-to-host copies of O, lse, dQ,
 dK, dV, all inside the timed region; the copies run on their own streams
-with two buffer sets, so one step's copies overlap its neighbours' compute.  `e2e_bf16_outputs` repeats it with bf16
-O, dQ, dK, dV (half the bytes read back).  `graph` times the same step captured
+with two buffer sets, so one step's copies overlap its neighbours' compute;
+the figure is the median of three runs (the host links are shared with the
+machine's other GPUs).  `e2e_bf16_outputs` repeats it with bf16 O, dQ, dK,
+dV (half the bytes read back).  `graph` times the same step captured
 once into a CUDA graph (fm_step_graph_create) and replayed, one launch per
 step.  `fp8_fwd` times the forward on e4m3 inputs (fm_attn_fwd_fp8) and the
 quantization of Q, K, V beside it.
@@ -396,8 +398,15 @@ def run_fm(args, rank, world, local_rank):
         del sets
         return sec, h2d, d2h
 
-    e2e_s, h2d, d2h = run_e2e(torch.float32)
-    e2e16_s, _, d2h16 = run_e2e(torch.bfloat16)
+    # The host links are shared with the machine's other GPUs, so one short run
+    # varies by tens of percent: three runs of each output type, alternating,
+    # and the median of each.
+    runs32, runs16 = [], []
+    for _ in range(3):
+        runs32.append(run_e2e(torch.float32))
+        runs16.append(run_e2e(torch.bfloat16))
+    e2e_s, h2d, d2h = sorted(runs32)[1]
+    e2e16_s, _, d2h16 = sorted(runs16)[1]
 
     ms_step, e2e_s, e2e16_s, graph_ms = max_over_ranks([ms_step, e2e_s, e2e16_s, graph_ms], world, dev)
     return dict(wl=wl, pairs=pairs, fwd_flops=fwd_flops, bwd_flops=bwd_flops, ms_step=ms_step,
