@@ -240,3 +240,65 @@ def test_profiler_records_every_launch(fm):
         rec = fm.fm_profile_end()
         assert [r[0] for r in rec] == head + tail, g_dtype
         assert all(ms > 0 for _, ms in rec)
+
+
+def test_partial_tile_warp_summaries(fm):
+    """A PARTIAL tile in which the first 32 rows (one softmax warp) are masked
+    in every column, rows 64-95 in some columns and the other rows in none, so
+    the forward's per-warp mask summary takes each of its three paths; another
+    tile with a lower-triangle mask and one without any.  Element by element
+    against the oracle, forward and backward."""
+    B, H, N, d = 1, 2, 384, 128
+    c = np.arange(N)
+    lts, lte = np.zeros(N, np.int32), np.zeros(N, np.int32)
+    uts, ute = np.zeros(N, np.int32), np.zeros(N, np.int32)
+    t0 = c < 128
+    lte[t0] = 32                                   # rows 0-31 in every column of KV tile 0
+    uts[t0] = 64
+    ute[t0] = 64 + c[t0] % 32                      # rows 64 .. 64 + c mod 32: mixed within rows 64-95
+    t1 = (c >= 128) & (c < 256)
+    lte[t1] = c[t1] - 128                          # KV tile 1: rows below c - 128
+    m = {key: arr.reshape(1, 1, N).copy() for key, arr in (("lts", lts), ("lte", lte), ("uts", uts), ("ute", ute))}
+    wl = W.Workload("warp_summaries", B=B, H=H, N=N, d=d, mask="full")
+    q, k, v, dO = W.make_inputs(wl, seed=11)
+    for flags in (0, 1):
+        out = run_fm(fm, wl, m, q, k, v, dO, flags=flags)
+        O, L = oracle.forward(q, k, v, m, wl.scale)
+        g = oracle.backward(q, k, v, dO, m, wl.scale)
+        check_all([("O", out["o"].cpu().numpy(), O), ("lse", out["lse"].cpu().numpy(), L),
+                   ("dQ", out["dq"].cpu().numpy(), g["dq"]), ("dK", out["dk"].cpu().numpy(), g["dk"]),
+                   ("dV", out["dv"].cpu().numpy(), g["dv"])])
+
+
+def test_unaligned_bound_arrays(fm):
+    """Bound arrays that start 4 bytes past a 16-byte boundary (the forward
+    then reads them one element at a time instead of in 16-byte loads) give
+    the oracle's result, forward and backward."""
+    wl = W.SMALL["lognormal_small"]
+    m = W.make_mask(wl)
+    q, k, v, dO = W.make_inputs(wl)
+    dev = torch.device("cuda")
+    att = fm.MaskedAttention(m["lts"], m["lte"], m["uts"], m["ute"], device=dev)
+    views = []
+    for key in ("lts", "lte", "uts", "ute"):
+        src = torch.from_numpy(np.ascontiguousarray(m[key])).reshape(-1)
+        buf = torch.zeros(src.numel() + 1, dtype=torch.int32, device=dev)
+        buf[1:] = src.to(dev)
+        views.append(buf[1:].view(m[key].shape))
+    assert all(t.data_ptr() % 16 != 0 for t in views)
+    bnd = fm.make_bounds(*views)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, dO))
+    B, H, N, d = q.shape
+    o = torch.full(q.shape, float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device=dev)
+    fm.fm_attn_fwd(qd, kd, vd, bnd, att.plan, wl.scale, o, lse, att.status)
+    ws = torch.empty(fm.fm_bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    gr = [torch.full(q.shape, float("nan"), dtype=torch.float32, device=dev) for _ in range(3)]
+    fm.fm_attn_bwd(qd, kd, vd, o, lse, dod, bnd, att.plan, wl.scale, *gr, ws, att.status)
+    torch.cuda.synchronize()
+    att.check_status()
+    O, L = oracle.forward(q, k, v, m, wl.scale)
+    g = oracle.backward(q, k, v, dO, m, wl.scale)
+    check_all([("O", o.cpu().numpy(), O), ("lse", lse.cpu().numpy(), L),
+               ("dQ", gr[0].cpu().numpy(), g["dq"]), ("dK", gr[1].cpu().numpy(), g["dk"]),
+               ("dV", gr[2].cpu().numpy(), g["dv"])])
