@@ -10,7 +10,8 @@ columns [s_r, s_{r+1}).  One step:
 
 1. all-gather the column bounds: every rank holds the whole O(N) mask;
 2. all-gather the K and V shards into full-length K, V in local memory (no
-   remote reads inside a kernel);
+   remote reads inside a kernel), while the rank's row window is classified
+   (once, for the forward and the backward);
 3. forward for the rank's rows against all keys (``fm_attn_fwd_rows``); the
    tile labels of the row window skip every key tile, hence every key shard,
    that those rows never attend;
@@ -93,6 +94,27 @@ def _gather_dim(local: torch.Tensor, splits, dim: int, group=None) -> torch.Tens
     return out.to(local.device) if staged else out
 
 
+def _gather_dim_start(local: torch.Tensor, splits, dim: int, group=None):
+    """Start the all-gather of ``_gather_dim`` without waiting for it; returns
+    a function that waits and assembles the full axis."""
+    world = len(splits) - 1
+    lens = [splits[r + 1] - splits[r] for r in range(world)]
+    pad_shape = list(local.shape)
+    pad_shape[dim] = max(lens)
+    staged = _host_staged(group, local)
+    send = local.new_zeros(pad_shape, device="cpu" if staged else local.device)
+    send.narrow(dim, 0, local.shape[dim]).copy_(local)
+    recv = [torch.empty_like(send) for _ in range(world)]
+    work = dist.all_gather(recv, send, group=group, async_op=True)
+
+    def finish() -> torch.Tensor:
+        work.wait()
+        out = torch.cat([recv[r].narrow(dim, 0, lens[r]) for r in range(world)], dim=dim).contiguous()
+        return out.to(local.device) if staged else out
+
+    return finish
+
+
 def reduce_scatter_rows(full: torch.Tensor, splits, rank: int, group=None) -> torch.Tensor:
     """Sum the ranks' full-length contributions [B, H, N, d] and return this
     rank's rows [B, H, L_r, d] of the sum: one reduce-scatter over pieces
@@ -144,20 +166,25 @@ class LibraryLocal:
         fm.fm_tile_classify_rows(bnd, q_row0, Nq, plan, status)
         return bnd, plan, status
 
-    def forward(self, q, k, v, bounds, q_row0, scale):
+    def prepare(self, bounds, q_row0, Nq):
+        """Classify the row window once (device work on the current stream);
+        the result serves the forward and the backward of the step."""
+        return self._plan(bounds, q_row0, Nq)
+
+    def forward(self, q, k, v, bounds, q_row0, scale, prep=None):
         fm = self.fm
         Nq = q.shape[2]
-        bnd, plan, status = self._plan(bounds, q_row0, Nq)
+        bnd, plan, status = prep if prep is not None else self._plan(bounds, q_row0, Nq)
         o = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         fm.fm_attn_fwd_rows(q, k, v, bnd, plan, q_row0, scale, o, lse, status, flags=self.flags)
         self._check(status)
         return o, lse
 
-    def backward(self, q, k, v, o, lse, dO, bounds, q_row0, scale):
+    def backward(self, q, k, v, o, lse, dO, bounds, q_row0, scale, prep=None):
         fm = self.fm
         B, H, Nq, d = q.shape
-        bnd, plan, status = self._plan(bounds, q_row0, Nq)
+        bnd, plan, status = prep if prep is not None else self._plan(bounds, q_row0, Nq)
         dq = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         dk = torch.empty(k.shape, dtype=torch.float32, device=q.device)
         dv = torch.empty(k.shape, dtype=torch.float32, device=q.device)
@@ -178,11 +205,16 @@ def step(q, k, v, dO, local_bounds, splits, rank, scale, local, group=None):
     rows [B, H, L_r, d]; local_bounds: the bounds of its columns [B, Hm, L_r].
     Returns O, lse, dQ, dK, dV of the rank's rows."""
     bounds = gather_bounds(local_bounds, splits, group)
-    k_full = gather_rows(k, splits, group)
-    v_full = gather_rows(v, splits, group)
+    # K and V move while the row window is classified (a computation with a
+    # ``prepare`` step does it once for the forward and the backward).
+    k_done = _gather_dim_start(k, splits, 2, group)
+    v_done = _gather_dim_start(v, splits, 2, group)
     q_row0 = splits[rank]
-    o, lse = local.forward(q, k_full, v_full, bounds, q_row0, scale)
-    dq, dk_part, dv_part = local.backward(q, k_full, v_full, o, lse, dO, bounds, q_row0, scale)
+    prep = local.prepare(bounds, q_row0, q.shape[2]) if hasattr(local, "prepare") else None
+    k_full, v_full = k_done(), v_done()
+    extra = {} if prep is None else {"prep": prep}
+    o, lse = local.forward(q, k_full, v_full, bounds, q_row0, scale, **extra)
+    dq, dk_part, dv_part = local.backward(q, k_full, v_full, o, lse, dO, bounds, q_row0, scale, **extra)
     dk = reduce_scatter_rows(dk_part, splits, rank, group)
     dv = reduce_scatter_rows(dv_part, splits, rank, group)
     return o, lse, dq, dk, dv
